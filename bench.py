@@ -1,0 +1,479 @@
+#!/usr/bin/env python
+"""Benchmark of the UniPrefill token-selection path on one GB300 (or N replicas).
+
+One step = one call of ``upf_select_tokens`` (score pass 1, score pass 2,
+finalize + block means, top-p select, compaction, drop-history append) over one
+batch of seeded synthetic inputs already resident in HBM.  Metric: prompt tokens
+scored + selected + compacted per second.  The default workload is the 128K
+LLaMA-3.1-8B-shaped full-attention layer (1 request, L=131072, H_q=32, H_kv=8,
+d=128, hidden 4096, n=128, G=64, p=0.99).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle on the host cores instead (the baseline arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from sparse_long_context_tail_gb300 import workload as wl  # noqa: E402
+
+METRIC = "prompt tokens scored+selected+compacted/sec at 128K"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "llama8b-L131072"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGES = ["describe", "score_pass1", "score_pass2", "finalize", "select", "compact_count", "compact_index",
+          "compact_gather"]
+# kernel sources per stage (for the traffic record's freshness check)
+STAGE_SOURCES = {"score_pass1": "score_simt.cu", "score_pass2": "score_simt.cu", "finalize": "select.cu",
+                 "select": "select.cu", "compact_gather": "compact.cu", "compact_index": "compact.cu",
+                 "compact_count": "compact.cu", "describe": "score_simt.cu"}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=wl.NAMED)
+    ap.add_argument("--top-p", type=float, default=None, help="override p (e.g. 1.0 keeps every token)")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ work counts ----
+
+def algorithmic_work(spec, cu, kept_total, row_bytes, top_p):
+    """Algorithmic flops / bytes per launch of each stage (what the method must do)."""
+    H_q, H_kv, d, n = spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.n_tail
+    L = np.diff(np.asarray(cu, dtype=np.int64))
+    T = int(L.sum())
+    vis = 0          # sum over requests and tail queries of visible keys (t_j + 1)
+    for x in L:
+        n_eff = min(n, int(x))
+        vis += n_eff * int(x) - n_eff * (n_eff - 1) // 2
+    flops_pass = 2.0 * d * H_q * vis
+    k_bytes = 2.0 * T * H_kv * d
+    q_bytes = 2.0 * H_q * d * sum(min(n, int(x)) for x in L)
+    nb = sum(-(-int(x) // spec.block) for x in L)
+    P = H_kv * max(1, math.ceil(H_q // H_kv * n / 512))
+    return {
+        "score_pass1": dict(bound="tensor", flops=flops_pass, bytes=k_bytes + q_bytes),
+        "score_pass2": dict(bound="tensor", flops=flops_pass, bytes=k_bytes + q_bytes + 4.0 * P * T),
+        "finalize": dict(bound="hbm", bytes=4.0 * P * T + 4.0 * T + 4.0 * nb + T / 8),
+        "select": dict(bound="latency", bytes=4.0 * nb + T / 8),
+        "compact_count": dict(bound="latency", bytes=T / 8),
+        "compact_index": dict(bound="latency", bytes=T / 8 + 4.0 * kept_total),
+        "compact_gather": dict(bound="hbm", bytes=kept_total * (2.0 * row_bytes + 32.0 + 4.0)),
+        "describe": dict(bound="latency", bytes=0.0),
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(stage):
+    src = os.path.join(ROOT, "sparse_long_context_tail_gb300", "csrc", STAGE_SOURCES.get(stage, ""))
+    if not os.path.isfile(src):
+        return None
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_record(stage, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it is still current."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+        r = rec.get(stage)
+        if r and r.get("workload") == workload and r.get("source_sha") == source_sha(stage):
+            return float(r["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        return None
+    return None
+
+
+# ----------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle ----
+
+def oracle_run(w, heads=None, threads=None):
+    """One pass of the float64 oracle over the workload (optionally a subset of q-heads for scoring).
+
+    Returns (score seconds, rest seconds, threads used)."""
+    import oracle
+    s = w.spec
+    thr = threads or min(32, os.cpu_count() or 1)
+    t0 = time.perf_counter()
+    if heads is None or heads >= s.num_q_heads:
+        scores = oracle.token_scores(w.k_bits, w.q_tail_bits, w.cu_seqlens, s.num_q_heads, s.num_kv_heads,
+                                     s.head_dim, s.n_tail, None, s.kv_of_q, thr)
+    else:
+        # the first `heads` q-heads (their kv heads follow the group map): a sample of the per-head work
+        gmap = s.group_map()
+        q = w.q_tail_bits[:, :heads, :]
+        scores = oracle.token_scores(w.k_bits, q, w.cu_seqlens, heads, s.num_kv_heads, s.head_dim, s.n_tail,
+                                     None, gmap[:heads].tolist(), thr)
+    t1 = time.perf_counter()
+    sel = oracle.select(scores, w.cu_seqlens, s.block, s.top_p, s.sink_keep, s.tail_keep)
+    oracle.compact(sel["mask"], w.cu_seqlens, w.hidden_bits(), w.positions(), w.slots(), 0)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1, thr
+
+
+def cpu_baseline(w, budget_s=15.0):
+    """Time the oracle as it stands on the host cores: whole passes until ~budget_s elapse (max 3)."""
+    runs = []
+    thr = None
+    t_start = time.perf_counter()
+    while len(runs) < 3:
+        ts, tr, thr = oracle_run(w)
+        runs.append(ts + tr)
+        if time.perf_counter() - t_start > budget_s:
+            break
+    per = statistics.median(runs)
+    return {"value": w.total_tokens / per, "unit": UNIT, "cores": thr, "kind": "oracle",
+            "sample": f"{len(runs)} full pass(es) of the float64 oracle over the whole workload "
+                      f"({w.spec.name}, {w.total_tokens} tokens, all {w.spec.num_q_heads} q-heads); "
+                      f"median {per:.2f} s per pass"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    spec = wl.named_spec(args.workload)
+    if args.top_p is not None:
+        spec.top_p = args.top_p
+    w = wl.generate(spec)
+    w.hidden_bits()
+    # Each step scores a sample of q-heads (the per-head work scales linearly) and
+    # runs selection + compaction in full; sized so warmup + steps stay within ~3 min.
+    t_score_1head, _, thr = oracle_run(w, heads=1)
+    per_step_budget = 150.0 / max(1, args.steps + args.warmup)
+    heads = int(max(1, min(spec.num_q_heads, per_step_budget / max(t_score_1head, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_run(w, heads=heads)
+    est = []
+    for _ in range(args.steps):
+        ts, tr, thr = oracle_run(w, heads=heads)
+        est.append(ts * spec.num_q_heads / heads + tr)
+    per = statistics.mean(est)
+    value = w.total_tokens / per
+    sample = (f"each step: float64 oracle scoring of {heads} of {spec.num_q_heads} q-heads (time scaled by "
+              f"{spec.num_q_heads}/{heads}) plus full selection and compaction of {spec.name}")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(spec, w, args), "gpu_launches": 0,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(spec, w, args):
+    return {"workload": spec.name, "requests": len(spec.lengths), "total_tokens": w.total_tokens,
+            "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
+            "hidden": spec.hidden, "n_tail": spec.n_tail, "block": spec.block, "top_p": spec.top_p,
+            "sink_keep": spec.sink_keep, "tail_keep": spec.tail_keep,
+            "l2": "flushed between steps (512 MiB write)" if not args.no_flush else "not flushed",
+            "parallelism": f"replicas x{args.gpus} (requests sharded per GPU, no collective)"}
+
+
+# ----------------------------------------------------------------- ours -----
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    from sparse_long_context_tail_gb300 import _binding as B
+    from sparse_long_context_tail_gb300.selector import TokenSelector
+
+    spec = wl.named_spec(args.workload)
+    if args.top_p is not None:
+        spec.top_p = args.top_p
+    t0 = time.time()
+    w = wl.generate(spec)
+    hidden_np = w.hidden_bits()
+    log(f"[bench] generated {spec.name} in {time.time() - t0:.1f} s")
+    cu = w.cu_seqlens
+    T = w.total_tokens
+    params = B.make_params(spec.n_tail, spec.block, spec.sink_keep, spec.tail_keep, spec.top_p)
+
+    # inputs resident in HBM
+    q_dev = torch.empty((T, spec.num_q_heads, spec.head_dim), dtype=torch.bfloat16, device=dev)
+    q_tail = torch.from_numpy(w.q_tail_bits.view(np.int16)).view(torch.bfloat16)
+    tail_idx = torch.from_numpy(w.tail_rows)
+    q_dev[tail_idx.to(dev)] = q_tail.to(dev)
+    k_dev = torch.from_numpy(w.k_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    hid_dev = torch.from_numpy(hidden_np.view(np.int16)).to(dev)
+    pos_dev = torch.from_numpy(w.positions()).to(dev)
+    slot_dev = torch.from_numpy(w.slots()).to(dev)
+    cu_dev = torch.from_numpy(cu).to(dev)
+    sel = TokenSelector(local)
+    out = sel.alloc_outputs(cu, spec.block, hid_dev, pos_dev, slot_dev)
+    flush = None if args.no_flush else torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def step(o=out):
+        return sel.select_tokens(q_dev, k_dev, cu, cu_dev, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                                 hid_dev, pos_dev, slot_dev, layer_id=0, params=params, kv_of_q=spec.kv_of_q,
+                                 out=o)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    status = sel.status()
+    if status != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES.get(status)} during warm-up")
+    kept_total = int(out.total_kept.item())
+
+    stream = torch.cuda.current_stream(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    B.upf_profile_read(sel.ctx)          # reset counters
+    B.upf_profile_enable(sel.ctx, True)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        if flush is not None:
+            flush.zero_()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    launches, stage_ms = B.upf_profile_read(sel.ctx)
+    B.upf_profile_enable(sel.ctx, False)
+    clk = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * T / (ms / 1e3)
+
+    # roofline of the dominant kernel (largest share of device time)
+    work = algorithmic_work(spec, cu, kept_total, hid_dev.stride(0) * 2, spec.top_p)
+    peaks, peak_kind = load_peaks()
+    tot_ms = sum(stage_ms) or 1.0
+    stages = {}
+    for i, nm in enumerate(STAGES):
+        n_l = max(1, launches[i])
+        per = stage_ms[i] / n_l
+        entry = {"launches": launches[i], "ms_per_launch": per, "share": stage_ms[i] / tot_ms}
+        wk = work[nm]
+        if per > 0:
+            if "flops" in wk:
+                entry["tflops"] = wk["flops"] / (per / 1e3) / 1e12
+            entry["gbs"] = wk["bytes"] / (per / 1e3) / 1e9
+        stages[nm] = entry
+    dom = max(range(len(STAGES)), key=lambda i: stage_ms[i])
+    dname = STAGES[dom]
+    dwork = work[dname]
+    dper = stage_ms[dom] / max(1, launches[dom]) / 1e3
+    if dwork["bound"] == "tensor":
+        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        achieved = dwork["flops"] / dper / 1e12
+        unit = "TFLOP/s"
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = dwork["bytes"] / dper / 1e9
+        unit = "GB/s"
+    traffic = traffic_record(dname, spec.name)
+    roofline = {"bound": "tensor" if dwork["bound"] == "tensor" else "hbm", "kernel": dname,
+                "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                "peak_source": f"{peak_kind} ({'bf16_tflops_sustained' if unit == 'TFLOP/s' else 'hbm_gbs'})",
+                "traffic": traffic}
+    if dwork["bound"] == "tensor":
+        roofline["algorithmic_flops_per_launch"] = dwork["flops"]
+    roofline["algorithmic_bytes_per_launch"] = dwork["bytes"]
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, torch, sel, spec, w, cu, params, q_dev, k_dev, hid_dev, pos_dev, slot_dev, cu_dev, out,
+                      dev, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded bf16 N(0,1) + planted blocks)",
+                "config": config_of(spec, w, args),
+                "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
+                "kept_tokens": kept_total, "kept_fraction": kept_total / T,
+                "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": int(sum(launches)), "clocks": clk, "wall_s": wall}
+        print(json.dumps(line), flush=True)
+    sel.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, torch, sel, spec, w, cu, params, q_dev, k_dev, hid_dev, pos_dev, slot_dev, cu_dev, out, dev, world):
+    """Same metric through TokenSelector.select_tokens with host (pinned) inputs and outputs."""
+    q_tail_h = torch.from_numpy(w.q_tail_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    tail_idx = torch.from_numpy(w.tail_rows).to(dev)
+    k_h = torch.from_numpy(w.k_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hid_h = torch.from_numpy(w.hidden_bits().view(np.int16)).pin_memory()
+    pos_h = torch.from_numpy(w.positions()).pin_memory()
+    slot_h = torch.from_numpy(w.slots()).pin_memory()
+    cu_h = torch.from_numpy(cu).pin_memory()
+    q_tail_d = torch.empty_like(q_tail_h, device=dev)
+    T = w.total_tokens
+    hout_h = torch.empty_like(hid_h).pin_memory()
+    pout_h = torch.empty_like(pos_h).pin_memory()
+    sout_h = torch.empty_like(slot_h).pin_memory()
+    bits_h = torch.empty_like(out.keep_bits, device="cpu").pin_memory()
+    cnt_h = torch.empty_like(out.kept_count, device="cpu").pin_memory()
+    cuo_h = torch.empty_like(out.cu_seqlens_out, device="cpu").pin_memory()
+    h2d = q_tail_h.numel() * 2 + k_h.numel() * 2 + hid_h.numel() * 2 + pos_h.numel() * 8 + slot_h.numel() * 8 + \
+        cu_h.numel() * 4
+    d2h_total = 0
+    times = []
+    for i in range(args.e2e_steps + 1):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        k_dev.copy_(k_h, non_blocking=True)
+        q_tail_d.copy_(q_tail_h, non_blocking=True)
+        q_dev.index_copy_(0, tail_idx, q_tail_d)
+        hid_dev.copy_(hid_h, non_blocking=True)
+        pos_dev.copy_(pos_h, non_blocking=True)
+        slot_dev.copy_(slot_h, non_blocking=True)
+        cu_dev.copy_(cu_h, non_blocking=True)
+        sel.select_tokens(q_dev, k_dev, cu, cu_dev, spec.num_q_heads, spec.num_kv_heads, spec.head_dim, hid_dev,
+                          pos_dev, slot_dev, layer_id=0, params=params, kv_of_q=spec.kv_of_q, out=out)
+        total = int(out.total_kept.item())
+        bits_h.copy_(out.keep_bits, non_blocking=True)
+        cnt_h.copy_(out.kept_count, non_blocking=True)
+        cuo_h.copy_(out.cu_seqlens_out, non_blocking=True)
+        hout_h[:total].copy_(out.hidden_out[:total], non_blocking=True)
+        pout_h[:total].copy_(out.pos_out[:total], non_blocking=True)
+        sout_h[:total].copy_(out.slot_out[:total], non_blocking=True)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        if i > 0:       # the first pass warms the pinned paths
+            times.append(dt)
+            d2h_total = 4 + bits_h.numel() * 4 + cnt_h.numel() * 4 + cuo_h.numel() * 4 + \
+                total * (hid_dev.stride(0) * 2 + 16)
+    per = statistics.mean(times)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([per], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        per = float(t.item())
+    return {"value": world * T / per, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h_total),
+            "ms_per_step": per * 1e3, "steps": len(times),
+            "note": "wall clock around pinned H2D of the step's inputs (K, tail Q rows, hidden, positions, slots, "
+                    "cu_seqlens), the call, and D2H of the mask, counts, offsets and the kept rows"}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,629 @@
+// libupf host side: argument checks, work planning, workspace layout and the
+// launch sequence of each C-ABI entry point declared in include/upf.h.
+//
+// Nothing here allocates except upf_create (one small device status word).
+// Every launch goes to the caller's stream; argument errors are reported before
+// the first launch.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "upf_internal.cuh"
+
+struct upf_ctx {
+  int device;
+  int num_sms;
+  int32_t* status_dev;  // [64] device words; [0] = status
+  // tracing
+  bool profiling = false;
+  int32_t launches[UPF_NUM_STAGES] = {};
+  struct Rec {
+    int stage;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> pending;
+  std::vector<cudaEvent_t> pool;
+
+  cudaEvent_t event() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+upf_status fail(upf_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+upf_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(UPF_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Everything the launches need that follows from the batch and parameters.
+struct Plan {
+  int R = 0, T = 0, Hq = 0, Hkv = 0, d = 0, gamma = 0;
+  int n = 0, G = 0, sink = 0, tail = 0;
+  float top_p = 0.f, scale = 0.f;
+  int QR = 0, QC = 0, NQC = 0, KS1 = 0, KS2 = 0;
+  long long items1 = 0, items2 = 0;
+  long long NB = 0;
+  int max_nb = 0;
+  int nwords = 0, nchunks = 0;
+  std::vector<int32_t> qhead;
+  // workspace offsets
+  size_t off_desc = 0, off_p1 = 0, off_part = 0, off_bs = 0, off_chunk = 0, off_kidx = 0, total = 0;
+};
+
+upf_status check_batch(const upf_batch* b) {
+  if (!b) return fail(UPF_ERR_INVALID_ARG, "batch is NULL");
+  if (b->num_reqs < 1) return fail(UPF_ERR_INVALID_ARG, "num_reqs must be >= 1 (got %d)", b->num_reqs);
+  if (!b->cu_seqlens_host || !b->cu_seqlens_dev)
+    return fail(UPF_ERR_INVALID_ARG, "cu_seqlens_host and cu_seqlens_dev are required");
+  if (b->cu_seqlens_host[0] != 0) return fail(UPF_ERR_INVALID_ARG, "cu_seqlens[0] must be 0");
+  for (int r = 0; r < b->num_reqs; ++r)
+    if (b->cu_seqlens_host[r + 1] < b->cu_seqlens_host[r])
+      return fail(UPF_ERR_INVALID_ARG, "cu_seqlens must be non-decreasing (r=%d)", r);
+  if (b->cu_seqlens_host[b->num_reqs] > (1 << 30))
+    return fail(UPF_ERR_UNSUPPORTED, "total tokens %d above 2^30", b->cu_seqlens_host[b->num_reqs]);
+  return UPF_OK;
+}
+
+upf_status check_heads(const upf_batch* b) {
+  if (b->num_q_heads < 1 || b->num_kv_heads < 1 || b->num_q_heads % b->num_kv_heads != 0)
+    return fail(UPF_ERR_INVALID_ARG, "need H_q %% H_kv == 0 and both >= 1 (got %d, %d)", b->num_q_heads,
+                b->num_kv_heads);
+  if (b->num_q_heads > upf::kMaxHeads)
+    return fail(UPF_ERR_UNSUPPORTED, "num_q_heads %d above %d", b->num_q_heads, upf::kMaxHeads);
+  if (b->head_dim != 64 && b->head_dim != 128 && b->head_dim != 256)
+    return fail(UPF_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256 (got %d)", b->head_dim);
+  if (b->kv_of_q) {
+    const int gamma = b->num_q_heads / b->num_kv_heads;
+    std::vector<int> cnt(b->num_kv_heads, 0);
+    for (int h = 0; h < b->num_q_heads; ++h) {
+      int g = b->kv_of_q[h];
+      if (g < 0 || g >= b->num_kv_heads) return fail(UPF_ERR_INVALID_ARG, "kv_of_q[%d]=%d out of range", h, g);
+      cnt[g]++;
+    }
+    for (int g = 0; g < b->num_kv_heads; ++g)
+      if (cnt[g] != gamma)
+        return fail(UPF_ERR_INVALID_ARG, "kv_of_q maps %d q heads to kv head %d, need %d", cnt[g], g, gamma);
+  }
+  return UPF_OK;
+}
+
+upf_status check_params(const upf_params* p) {
+  if (!p) return fail(UPF_ERR_INVALID_ARG, "params is NULL");
+  if (p->n_tail < 1 || p->n_tail > 4096) return fail(UPF_ERR_UNSUPPORTED, "n_tail must be in [1, 4096]");
+  if (p->block < 1 || p->block > (1 << 20)) return fail(UPF_ERR_INVALID_ARG, "block must be in [1, 2^20]");
+  if (p->sink_keep < 0 || p->tail_keep < 0) return fail(UPF_ERR_INVALID_ARG, "sink_keep/tail_keep must be >= 0");
+  if (!(p->top_p > 0.f && p->top_p <= 1.f)) return fail(UPF_ERR_INVALID_ARG, "top_p must be in (0, 1]");
+  if (!std::isfinite(p->softmax_scale)) return fail(UPF_ERR_INVALID_ARG, "softmax_scale must be finite");
+  return UPF_OK;
+}
+
+int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
+
+// Keys per split so that the pass has about `target` items in total.
+int choose_split(const upf_batch* b, int per_req_units, long long target) {
+  long long keys = 0;
+  for (int r = 0; r < b->num_reqs; ++r) keys += b->cu_seqlens_host[r + 1] - b->cu_seqlens_host[r];
+  long long units = keys * per_req_units;
+  long long ks = (units + target - 1) / std::max(1LL, target);
+  ks = ((ks + 127) / 128) * 128;
+  if (ks < 256) ks = 256;
+  return int(std::min<long long>(ks, 1 << 30));
+}
+
+upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p, bool need_heads, Plan* pl) {
+  upf_status st = check_batch(b);
+  if (st != UPF_OK) return st;
+  if (need_heads) {
+    if ((st = check_heads(b)) != UPF_OK) return st;
+    if ((st = check_params(p)) != UPF_OK) return st;
+  }
+  pl->R = b->num_reqs;
+  pl->T = b->cu_seqlens_host[b->num_reqs];
+  if (need_heads) {
+    pl->Hq = b->num_q_heads;
+    pl->Hkv = b->num_kv_heads;
+    pl->d = b->head_dim;
+    pl->gamma = pl->Hq / pl->Hkv;
+    pl->n = p->n_tail;
+    pl->G = p->block;
+    pl->sink = p->sink_keep;
+    pl->tail = p->tail_keep;
+    pl->top_p = p->top_p;
+    pl->scale = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / std::sqrt(float(b->head_dim));
+    pl->QR = pl->gamma * pl->n;
+    const int qc_max = 512;
+    pl->QC = std::min(pl->QR, qc_max);
+    pl->NQC = ceil_div(pl->QR, pl->QC);
+    // The split depends only on the batch and parameters (never on the device),
+    // so upf_workspace_bytes() without a context sizes exactly what a call uses.
+    (void)ctx;
+    pl->KS1 = choose_split(b, pl->Hkv * pl->NQC, 2LL * upf::kPlanSMs);
+    pl->KS2 = choose_split(b, pl->Hkv * pl->NQC, 4LL * upf::kPlanSMs);
+    pl->items1 = pl->items2 = 0;
+    pl->NB = 0;
+    pl->max_nb = 0;
+    for (int r = 0; r < pl->R; ++r) {
+      int L = b->cu_seqlens_host[r + 1] - b->cu_seqlens_host[r];
+      pl->items1 += (long long)pl->Hkv * pl->NQC * ceil_div(L, pl->KS1);
+      pl->items2 += (long long)pl->Hkv * pl->NQC * ceil_div(L, pl->KS2);
+      int nb = ceil_div(L, pl->G);
+      pl->NB += nb;
+      pl->max_nb = std::max(pl->max_nb, nb);
+    }
+    if (pl->max_nb > upf::kMaxBlocksPerReq)
+      return fail(UPF_ERR_UNSUPPORTED, "a request has %d blocks; at most %d are supported", pl->max_nb,
+                  upf::kMaxBlocksPerReq);
+    if (pl->items1 > (1LL << 30) || pl->items2 > (1LL << 30)) return fail(UPF_ERR_UNSUPPORTED, "batch too large");
+    pl->qhead.assign(pl->Hq, 0);
+    std::vector<int> fill(pl->Hkv, 0);
+    for (int h = 0; h < pl->Hq; ++h) {
+      int g = b->kv_of_q ? b->kv_of_q[h] : h / pl->gamma;
+      pl->qhead[g * pl->gamma + fill[g]++] = h;
+    }
+  }
+  pl->nwords = ceil_div(pl->T, 32);
+  pl->nchunks = std::max(1, ceil_div(pl->nwords, upf::kCompactChunkWords));
+  size_t off = 0;
+  pl->off_desc = off;
+  off = align256(off + sizeof(int32_t) * 3 * (pl->R + 1));
+  pl->off_p1 = off;
+  off = align256(off + sizeof(float2) * size_t(pl->items1) * pl->QC);
+  pl->off_part = off;
+  off = align256(off + sizeof(float) * size_t(pl->Hkv) * pl->NQC * pl->T);
+  pl->off_bs = off;
+  off = align256(off + sizeof(float) * size_t(pl->NB));
+  pl->off_chunk = off;
+  off = align256(off + sizeof(int32_t) * pl->nchunks);
+  pl->off_kidx = off;
+  off = align256(off + sizeof(int32_t) * size_t(pl->T));
+  pl->total = off;
+  return UPF_OK;
+}
+
+upf_status check_ws(const Plan& pl, void* ws, size_t ws_bytes) {
+  if (!ws) return fail(UPF_ERR_INVALID_ARG, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % 256) return fail(UPF_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (ws_bytes < pl.total)
+    return fail(UPF_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", ws_bytes, pl.total);
+  return UPF_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+upf_status check_ctx(const upf_ctx* ctx) {
+  if (!ctx) return fail(UPF_ERR_INVALID_ARG, "context is NULL");
+  return UPF_OK;
+}
+
+upf_status check_score_io(const Plan& pl, const void* q, int64_t qs, const void* k, int64_t ks) {
+  if (!q || !k) return fail(UPF_ERR_INVALID_ARG, "q and k are required");
+  if (!aligned16(q) || !aligned16(k)) return fail(UPF_ERR_INVALID_ARG, "q and k must be 16-byte aligned");
+  if (qs < (int64_t)pl.Hq * pl.d || qs % 8) return fail(UPF_ERR_INVALID_ARG, "q_row_stride must be >= H_q*d and a multiple of 8");
+  if (ks < (int64_t)pl.Hkv * pl.d || ks % 8) return fail(UPF_ERR_INVALID_ARG, "k_row_stride must be >= H_kv*d and a multiple of 8");
+  return UPF_OK;
+}
+
+upf_status check_compact_io(const Plan& pl, const uint32_t* keep_bits, const upf_compact_io* io) {
+  if (!keep_bits) return fail(UPF_ERR_INVALID_ARG, "keep_bits is NULL");
+  if (!io) return fail(UPF_ERR_INVALID_ARG, "compact io is NULL");
+  if (!io->cu_seqlens_out || !io->total_kept) return fail(UPF_ERR_INVALID_ARG, "cu_seqlens_out and total_kept are required");
+  if (!io->hidden_in != !io->hidden_out) return fail(UPF_ERR_INVALID_ARG, "hidden_in/hidden_out must both be set or both NULL");
+  if (!io->pos_in != !io->pos_out) return fail(UPF_ERR_INVALID_ARG, "pos_in/pos_out must both be set or both NULL");
+  if (!io->slot_in != !io->slot_out) return fail(UPF_ERR_INVALID_ARG, "slot_in/slot_out must both be set or both NULL");
+  if (io->hidden_in) {
+    if (io->row_bytes <= 0 || io->row_bytes % 16) return fail(UPF_ERR_INVALID_ARG, "row_bytes must be a positive multiple of 16");
+    if (!aligned16(io->hidden_in) || !aligned16(io->hidden_out))
+      return fail(UPF_ERR_INVALID_ARG, "hidden buffers must be 16-byte aligned");
+  }
+  if (!io->history != !io->history_len) return fail(UPF_ERR_INVALID_ARG, "history/history_len must both be set or both NULL");
+  if (io->history && io->history_cap < 1) return fail(UPF_ERR_INVALID_ARG, "history_cap must be >= 1");
+  (void)pl;
+  return UPF_OK;
+}
+
+upf::ScoreArgs score_args(const upf_ctx* ctx, const upf_batch* b, const Plan& pl, const void* q, int64_t qs,
+                          const void* k, int64_t ks, void* ws) {
+  upf::ScoreArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.q_stride = qs;
+  a.k_stride = ks;
+  a.cu = b->cu_seqlens_dev;
+  a.R = pl.R;
+  a.T = pl.T;
+  a.Hq = pl.Hq;
+  a.Hkv = pl.Hkv;
+  a.d = pl.d;
+  a.n = pl.n;
+  a.gamma = pl.gamma;
+  a.QR = pl.QR;
+  a.QC = pl.QC;
+  a.NQC = pl.NQC;
+  a.KS1 = pl.KS1;
+  a.KS2 = pl.KS2;
+  a.items1 = int(pl.items1);
+  a.items2 = int(pl.items2);
+  a.scale_log2 = pl.scale * 1.4426950408889634f;
+  a.item_off1 = at<int32_t>(ws, pl.off_desc);
+  a.item_off2 = at<int32_t>(ws, pl.off_desc) + (pl.R + 1);
+  a.p1part = at<float2>(ws, pl.off_p1);
+  a.part = at<float>(ws, pl.off_part);
+  a.status = ctx->status_dev;
+  for (int i = 0; i < pl.Hq; ++i) a.qhead[i] = pl.qhead[i];
+  return a;
+}
+
+upf::DescribeArgs describe_args(const upf_ctx* ctx, const upf_batch* b, const Plan& pl, void* ws) {
+  upf::DescribeArgs a;
+  a.cu = b->cu_seqlens_dev;
+  a.R = pl.R;
+  a.T = pl.T;
+  a.Hkv = pl.Hkv;
+  a.NQC = pl.NQC;
+  a.KS1 = pl.KS1;
+  a.KS2 = pl.KS2;
+  a.G = pl.G;
+  a.items1 = int(pl.items1);
+  a.items2 = int(pl.items2);
+  a.NB = int(pl.NB);
+  a.item_off1 = at<int32_t>(ws, pl.off_desc);
+  a.item_off2 = a.item_off1 + (pl.R + 1);
+  a.blk_off = a.item_off2 + (pl.R + 1);
+  a.status = ctx->status_dev;
+  return a;
+}
+
+upf::SelectArgs select_args(const upf_ctx* ctx, const upf_batch* b, const Plan& pl, void* ws, int P,
+                            const float* part, const float* scores_in, float* scores_out, float* block_scores,
+                            uint32_t* keep_bits, int32_t* kept_count) {
+  upf::SelectArgs a;
+  a.cu = b->cu_seqlens_dev;
+  a.R = pl.R;
+  a.T = pl.T;
+  a.G = pl.G;
+  a.sink_keep = pl.sink;
+  a.tail_keep = pl.tail;
+  a.n = pl.n;
+  a.Hq = pl.Hq;
+  a.NB = int(pl.NB);
+  a.max_nb = pl.max_nb;
+  a.P = P;
+  a.top_p = pl.top_p;
+  a.part = part;
+  a.scores_in = scores_in;
+  a.scores_out = scores_out;
+  a.block_scores = block_scores ? block_scores : at<float>(ws, pl.off_bs);
+  a.blk_off = at<int32_t>(ws, pl.off_desc) + 2 * (pl.R + 1);
+  a.keep_bits = keep_bits;
+  a.kept_count = kept_count;
+  a.status = ctx->status_dev;
+  return a;
+}
+
+upf::CompactArgs compact_args(const upf_ctx* ctx, const upf_batch* b, const Plan& pl, const uint32_t* keep_bits,
+                              const upf_compact_io* io, void* ws) {
+  upf::CompactArgs a;
+  a.cu = b->cu_seqlens_dev;
+  a.R = pl.R;
+  a.T = pl.T;
+  a.nwords = pl.nwords;
+  a.nchunks = pl.nchunks;
+  a.keep_bits = keep_bits;
+  a.chunk_tot = at<int32_t>(ws, pl.off_chunk);
+  a.kept_index = io->kept_index ? io->kept_index : at<int32_t>(ws, pl.off_kidx);
+  a.row_bytes = io->hidden_in ? io->row_bytes : 0;
+  a.hidden_in = io->hidden_in;
+  a.hidden_out = io->hidden_out;
+  a.pos_in = io->pos_in;
+  a.pos_out = io->pos_out;
+  a.slot_in = io->slot_in;
+  a.slot_out = io->slot_out;
+  a.cu_out = io->cu_seqlens_out;
+  a.total_kept = io->total_kept;
+  a.layer_id = io->layer_id;
+  a.history_cap = io->history_cap;
+  a.history = io->history;
+  a.history_len = io->history_len;
+  a.status = ctx->status_dev;
+  return a;
+}
+
+#define UPF_LAUNCH(expr, what)                       \
+  do {                                               \
+    cudaError_t e_ = (expr);                         \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+// Launch `f` as stage `stage`: counted always, bracketed by events when tracing.
+template <class F>
+cudaError_t staged(upf_ctx* ctx, int stage, cudaStream_t s, F&& f) {
+  ctx->launches[stage]++;
+  if (!ctx->profiling) return f();
+  cudaEvent_t a = ctx->event(), b = ctx->event();
+  if (!a || !b) return cudaErrorMemoryAllocation;
+  cudaEventRecord(a, s);
+  cudaError_t e = f();
+  cudaEventRecord(b, s);
+  ctx->pending.push_back({stage, a, b});
+  return e;
+}
+
+enum Stage { kDescribe = 0, kPass1, kPass2, kFinalize, kSelect, kCompactCount, kCompactIndex, kCompactGather };
+
+upf_status launch_compact_all(upf_ctx* ctx, const upf::CompactArgs& ca, cudaStream_t s) {
+  UPF_LAUNCH(staged(ctx, kCompactCount, s, [&] { return upf::launch_compact_count(ca, s); }), "compact count");
+  UPF_LAUNCH(staged(ctx, kCompactIndex, s, [&] { return upf::launch_compact_index(ca, s); }), "compact index");
+  UPF_LAUNCH(staged(ctx, kCompactGather, s, [&] { return upf::launch_compact_gather(ca, s); }), "compact gather");
+  return UPF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int upf_version(void) { return UPF_VERSION; }
+
+void upf_default_params(upf_params* p) {
+  if (!p) return;
+  p->n_tail = 128;
+  p->block = 64;
+  p->sink_keep = 128;
+  p->tail_keep = 128;
+  p->top_p = 0.99f;
+  p->softmax_scale = 0.f;
+}
+
+const char* upf_status_name(upf_status s) {
+  switch (s) {
+    case UPF_OK: return "UPF_OK";
+    case UPF_ERR_INVALID_ARG: return "UPF_ERR_INVALID_ARG";
+    case UPF_ERR_UNSUPPORTED: return "UPF_ERR_UNSUPPORTED";
+    case UPF_ERR_CUDA: return "UPF_ERR_CUDA";
+    case UPF_ERR_CAPACITY: return "UPF_ERR_CAPACITY";
+    case UPF_ERR_NONFINITE: return "UPF_ERR_NONFINITE";
+    case UPF_ERR_TIMEOUT: return "UPF_ERR_TIMEOUT";
+  }
+  return "UPF_ERR_UNKNOWN";
+}
+
+const char* upf_last_error(void) { return g_last_error.c_str(); }
+
+upf_status upf_create(upf_ctx** out, int device) {
+  if (!out) return fail(UPF_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  int count = 0;
+  cudaError_t e = cudaGetDeviceCount(&count);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+  if (device < 0 || device >= count) return fail(UPF_ERR_INVALID_ARG, "device %d out of range (%d devices)", device, count);
+  DeviceGuard guard(device);
+  if (!guard.ok) return fail(UPF_ERR_CUDA, "cudaSetDevice(%d) failed", device);
+  upf_ctx* c = new upf_ctx();
+  c->device = device;
+  if ((e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess) {
+    delete c;
+    return cuda_fail(e, "cudaDeviceGetAttribute");
+  }
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+  if (major * 10 + minor != 103) {
+    delete c;
+    return fail(UPF_ERR_UNSUPPORTED, "libupf is built for sm_103a; device %d is sm_%d%d", device, major, minor);
+  }
+  if ((e = cudaMalloc(&c->status_dev, 64 * sizeof(int32_t))) != cudaSuccess) {
+    delete c;
+    return cuda_fail(e, "cudaMalloc(status)");
+  }
+  if ((e = cudaMemset(c->status_dev, 0, 64 * sizeof(int32_t))) != cudaSuccess) {
+    cudaFree(c->status_dev);
+    delete c;
+    return cuda_fail(e, "cudaMemset(status)");
+  }
+  *out = c;
+  return UPF_OK;
+}
+
+upf_status upf_destroy(upf_ctx* ctx) {
+  if (!ctx) return fail(UPF_ERR_INVALID_ARG, "context is NULL");
+  DeviceGuard guard(ctx->device);
+  for (auto& r : ctx->pending) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : ctx->pool) cudaEventDestroy(e);
+  cudaFree(ctx->status_dev);
+  delete ctx;
+  return UPF_OK;
+}
+
+upf_status upf_sync_status(upf_ctx* ctx, void* stream) {
+  upf_status st = check_ctx(ctx);
+  if (st != UPF_OK) return st;
+  DeviceGuard guard(ctx->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int32_t code = 0;
+  if ((e = cudaMemcpy(&code, ctx->status_dev, sizeof(code), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "read status");
+  if (code != 0) {
+    if ((e = cudaMemset(ctx->status_dev, 0, sizeof(int32_t))) != cudaSuccess) return cuda_fail(e, "reset status");
+    return fail(static_cast<upf_status>(code), "device reported %s", upf_status_name(static_cast<upf_status>(code)));
+  }
+  return UPF_OK;
+}
+
+const char* upf_stage_name(int32_t stage) {
+  static const char* names[UPF_NUM_STAGES] = {"describe",       "score_pass1",   "score_pass2",  "finalize",
+                                              "select",         "compact_count", "compact_index", "compact_gather"};
+  return (stage >= 0 && stage < UPF_NUM_STAGES) ? names[stage] : "";
+}
+
+upf_status upf_profile_enable(upf_ctx* ctx, int32_t on) {
+  upf_status st = check_ctx(ctx);
+  if (st != UPF_OK) return st;
+  ctx->profiling = on != 0;
+  return UPF_OK;
+}
+
+upf_status upf_profile_read(upf_ctx* ctx, int32_t* launches, double* ms, int32_t n_stages) {
+  upf_status st = check_ctx(ctx);
+  if (st != UPF_OK) return st;
+  if (n_stages < 0 || n_stages > UPF_NUM_STAGES) return fail(UPF_ERR_INVALID_ARG, "n_stages must be in [0, %d]", UPF_NUM_STAGES);
+  DeviceGuard guard(ctx->device);
+  double acc[UPF_NUM_STAGES] = {};
+  cudaError_t err = cudaSuccess;
+  for (auto& r : ctx->pending) {
+    cudaError_t e = cudaEventSynchronize(r.b);
+    float t = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.a, r.b);
+    if (e != cudaSuccess && err == cudaSuccess) err = e;
+    acc[r.stage] += t;
+    ctx->pool.push_back(r.a);
+    ctx->pool.push_back(r.b);
+  }
+  ctx->pending.clear();
+  for (int i = 0; i < n_stages; ++i) {
+    if (launches) launches[i] = ctx->launches[i];
+    if (ms) ms[i] = acc[i];
+  }
+  for (int i = 0; i < UPF_NUM_STAGES; ++i) ctx->launches[i] = 0;
+  if (err != cudaSuccess) return cuda_fail(err, "profile events");
+  return UPF_OK;
+}
+
+size_t upf_workspace_bytes(const upf_batch* batch, const upf_params* params) {
+  Plan pl;
+  if (make_plan(nullptr, batch, params, true, &pl) != UPF_OK) return 0;
+  return pl.total;
+}
+
+upf_status upf_score(upf_ctx* ctx, const upf_batch* batch, const upf_params* params, const void* q,
+                     int64_t q_row_stride, const void* k, int64_t k_row_stride, float* scores, void* ws,
+                     size_t ws_bytes, void* stream) {
+  upf_status st;
+  if ((st = check_ctx(ctx)) != UPF_OK) return st;
+  Plan pl;
+  if ((st = make_plan(ctx, batch, params, true, &pl)) != UPF_OK) return st;
+  if ((st = check_ws(pl, ws, ws_bytes)) != UPF_OK) return st;
+  if ((st = check_score_io(pl, q, q_row_stride, k, k_row_stride)) != UPF_OK) return st;
+  if (!scores) return fail(UPF_ERR_INVALID_ARG, "scores is NULL");
+  DeviceGuard guard(ctx->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const upf::DescribeArgs da = describe_args(ctx, batch, pl, ws);
+  UPF_LAUNCH(staged(ctx, kDescribe, s, [&] { return upf::launch_describe(da, s); }), "describe");
+  upf::ScoreArgs sa = score_args(ctx, batch, pl, q, q_row_stride, k, k_row_stride, ws);
+  UPF_LAUNCH(staged(ctx, kPass1, s, [&] { return upf::launch_score_pass1(sa, s); }), "score pass 1");
+  UPF_LAUNCH(staged(ctx, kPass2, s, [&] { return upf::launch_score_pass2(sa, s); }), "score pass 2");
+  upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC, sa.part, nullptr, scores, nullptr,
+                                   nullptr, nullptr);
+  UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s); }), "finalize scores");
+  return UPF_OK;
+}
+
+upf_status upf_select(upf_ctx* ctx, const upf_batch* batch, const upf_params* params, const float* scores,
+                      float* block_scores, uint32_t* keep_bits, int32_t* kept_count, void* ws, size_t ws_bytes,
+                      void* stream) {
+  upf_status st;
+  if ((st = check_ctx(ctx)) != UPF_OK) return st;
+  Plan pl;
+  if ((st = make_plan(ctx, batch, params, true, &pl)) != UPF_OK) return st;
+  if ((st = check_ws(pl, ws, ws_bytes)) != UPF_OK) return st;
+  if (!scores || !keep_bits || !kept_count) return fail(UPF_ERR_INVALID_ARG, "scores, keep_bits and kept_count are required");
+  DeviceGuard guard(ctx->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const upf::DescribeArgs da = describe_args(ctx, batch, pl, ws);
+  UPF_LAUNCH(staged(ctx, kDescribe, s, [&] { return upf::launch_describe(da, s); }), "describe");
+  upf::SelectArgs se = select_args(ctx, batch, pl, ws, 0, nullptr, scores, nullptr, block_scores, keep_bits,
+                                   kept_count);
+  UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s); }), "block means");
+  UPF_LAUNCH(staged(ctx, kSelect, s, [&] { return upf::launch_select(se, s); }), "select");
+  return UPF_OK;
+}
+
+upf_status upf_compact(upf_ctx* ctx, const upf_batch* batch, const uint32_t* keep_bits, const upf_compact_io* io,
+                       void* ws, size_t ws_bytes, void* stream) {
+  upf_status st;
+  if ((st = check_ctx(ctx)) != UPF_OK) return st;
+  Plan pl;
+  if ((st = make_plan(ctx, batch, nullptr, false, &pl)) != UPF_OK) return st;
+  if ((st = check_ws(pl, ws, ws_bytes)) != UPF_OK) return st;
+  if ((st = check_compact_io(pl, keep_bits, io)) != UPF_OK) return st;
+  DeviceGuard guard(ctx->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return launch_compact_all(ctx, compact_args(ctx, batch, pl, keep_bits, io, ws), s);
+  return UPF_OK;
+}
+
+upf_status upf_select_tokens(upf_ctx* ctx, const upf_batch* batch, const upf_params* params, const void* q,
+                             int64_t q_row_stride, const void* k, int64_t k_row_stride, float* scores,
+                             float* block_scores, uint32_t* keep_bits, int32_t* kept_count,
+                             const upf_compact_io* io, void* ws, size_t ws_bytes, void* stream) {
+  upf_status st;
+  if ((st = check_ctx(ctx)) != UPF_OK) return st;
+  Plan pl;
+  if ((st = make_plan(ctx, batch, params, true, &pl)) != UPF_OK) return st;
+  if ((st = check_ws(pl, ws, ws_bytes)) != UPF_OK) return st;
+  if ((st = check_score_io(pl, q, q_row_stride, k, k_row_stride)) != UPF_OK) return st;
+  if (!keep_bits || !kept_count) return fail(UPF_ERR_INVALID_ARG, "keep_bits and kept_count are required");
+  if ((st = check_compact_io(pl, keep_bits, io)) != UPF_OK) return st;
+  DeviceGuard guard(ctx->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const upf::DescribeArgs da = describe_args(ctx, batch, pl, ws);
+  UPF_LAUNCH(staged(ctx, kDescribe, s, [&] { return upf::launch_describe(da, s); }), "describe");
+  upf::ScoreArgs sa = score_args(ctx, batch, pl, q, q_row_stride, k, k_row_stride, ws);
+  UPF_LAUNCH(staged(ctx, kPass1, s, [&] { return upf::launch_score_pass1(sa, s); }), "score pass 1");
+  UPF_LAUNCH(staged(ctx, kPass2, s, [&] { return upf::launch_score_pass2(sa, s); }), "score pass 2");
+  upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC, sa.part, nullptr, scores, block_scores,
+                                   keep_bits, kept_count);
+  UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s); }), "finalize scores");
+  UPF_LAUNCH(staged(ctx, kSelect, s, [&] { return upf::launch_select(se, s); }), "select");
+  return launch_compact_all(ctx, compact_args(ctx, batch, pl, keep_bits, io, ws), s);
+  return UPF_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+// Internal declarations shared by the libupf host code and its kernels.
+//
+// Work decomposition of the two scoring passes (UniPrefill article, section 二
+// first step; section 三, scores + online normalisation):
+//   * query rows of kv-group g: rho in [0, QR), QR = gamma * n; row rho is the
+//     tail query j = rho % n of the q-head qhead[g*gamma + rho / n]; its
+//     position in the request is t = L - n + j and it exists only if t >= 0.
+//   * the rows of a group are cut into NQC chunks of QC rows;
+//   * keys of request r are cut into splits of KS1 (pass 1) / KS2 (pass 2) keys;
+//   * an item is (request r, kv head g, query chunk qc, key split s), numbered
+//     request-major; item_off[r] is the first item of request r.
+// Pass 1 writes per item and row the partial (m2, Z): m2 = max over the item's
+// visible keys of x = scale*log2(e)*(q.k), Z = sum 2^(x - m2).  Pass 2 merges
+// the partials of (r, g, qc) into lse2 = m2 + log2 Z and accumulates
+// sum_rows 2^(x - lse2) per key into part[g*NQC + qc][token].
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/upf.h"
+
+namespace upf {
+
+constexpr int kMaxHeads = 256;         // H_q limit (the q-head list travels by value)
+constexpr int kMaxBlocksPerReq = 16384;  // select kernel sorts up to this many blocks in shared memory
+constexpr int kCompactChunkWords = 1024;  // keep-bit words per compaction chunk (32768 tokens)
+constexpr int kPlanSMs = 152;             // SM count the work split is planned for (GB300)
+
+struct ScoreArgs {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  int64_t q_stride;      // elements between consecutive tokens of q
+  int64_t k_stride;      // elements between consecutive tokens of k
+  const int32_t* cu;     // device cu_seqlens [R+1]
+  int32_t R, T, Hq, Hkv, d, n, gamma;
+  int32_t QR, QC, NQC;
+  int32_t KS1, KS2;
+  int32_t items1, items2;  // host totals (grid sizes)
+  float scale_log2;
+  const int32_t* item_off1;  // [R+1]
+  const int32_t* item_off2;  // [R+1]
+  float2* p1part;            // [items1][QC]
+  float* part;               // [Hkv*NQC][T]
+  int32_t* status;
+  int32_t qhead[kMaxHeads];  // q heads of group g at [g*gamma, (g+1)*gamma)
+};
+
+struct DescribeArgs {
+  const int32_t* cu;
+  int32_t R, T, Hkv, NQC, KS1, KS2, G;
+  int32_t items1, items2, NB;  // host totals: the device-derived ones must match
+  int32_t* item_off1;
+  int32_t* item_off2;
+  int32_t* blk_off;
+  int32_t* status;
+};
+
+struct SelectArgs {
+  const int32_t* cu;
+  int32_t R, T, G, sink_keep, tail_keep, n;
+  int32_t Hq;
+  int32_t NB;             // total blocks (host value)
+  int32_t max_nb;         // largest per-request block count (host value)
+  int32_t P;              // partial rows in part (0 = read `scores`)
+  float top_p;
+  const float* part;      // [P][T] (fused path)
+  const float* scores_in; // [T] (upf_select path)
+  float* scores_out;      // [T] or null (fused path)
+  float* block_scores;    // [NB]
+  const int32_t* blk_off; // [R+1]
+  uint32_t* keep_bits;    // [ceil(T/32)]
+  int32_t* kept_count;    // [R]
+  int32_t* status;
+};
+
+struct CompactArgs {
+  const int32_t* cu;
+  int32_t R, T, nwords, nchunks;
+  const uint32_t* keep_bits;
+  int32_t* chunk_tot;     // [nchunks]
+  int32_t* kept_index;    // [T]
+  int64_t row_bytes;
+  const void* hidden_in;
+  void* hidden_out;
+  const int64_t* pos_in;
+  int64_t* pos_out;
+  const int64_t* slot_in;
+  int64_t* slot_out;
+  int32_t* cu_out;
+  int32_t* total_kept;
+  int32_t layer_id, history_cap;
+  int32_t* history;
+  int32_t* history_len;
+  int32_t* status;
+};
+
+// Device status word helpers: the first error code wins.
+__device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Launchers (defined in the kernel translation units); all return cudaGetLastError().
+cudaError_t launch_describe(const DescribeArgs& a, cudaStream_t s);
+cudaError_t launch_score_pass1(const ScoreArgs& a, cudaStream_t s);
+cudaError_t launch_score_pass2(const ScoreArgs& a, cudaStream_t s);
+cudaError_t launch_block_means(const SelectArgs& a, cudaStream_t s);
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
+cudaError_t launch_compact_count(const CompactArgs& a, cudaStream_t s);
+cudaError_t launch_compact_index(const CompactArgs& a, cudaStream_t s);
+cudaError_t launch_compact_gather(const CompactArgs& a, cudaStream_t s);
+
+}  // namespace upf

@@ -1,0 +1,97 @@
+"""The C ABI without a GPU: the library builds, loads, exports every declared
+entry point, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from sparse_long_context_tail_gb300 import _binding as B
+from sparse_long_context_tail_gb300 import build as build_mod
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "upf.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(upf_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in B._SIGNATURES, f"binding lacks {n}"
+
+
+def test_version_and_defaults(lib):
+    assert B.upf_version() == 1
+    p = B.upf_default_params()
+    assert (p.n_tail, p.block, p.sink_keep, p.tail_keep) == (128, 64, 128, 128)
+    assert abs(p.top_p - 0.99) < 1e-7 and p.softmax_scale == 0.0
+    assert B.upf_status_name(0) == "UPF_OK" and B.upf_status_name(4) == "UPF_ERR_CAPACITY"
+
+
+def _batch(cu, Hq=32, Hkv=8, d=128, kv=None):
+    return B.make_batch(0x1000, np.asarray(cu, np.int32), Hq, Hkv, d, kv)
+
+
+def test_workspace_bytes_valid_and_invalid(lib):
+    b, keep = _batch([0, 131072])
+    n = B.upf_workspace_bytes(b, B.make_params())
+    assert n > 131072 * 8 * 4    # at least the per-group partial scores
+    b2, k2 = _batch([0, 5000, 9000])
+    assert B.upf_workspace_bytes(b2, B.make_params()) > 0
+    bad = [(_batch([0, 100], Hq=6, Hkv=4), B.make_params(), "H_q"),
+           (_batch([0, 100], d=96), B.make_params(), "head_dim"),
+           (_batch([0, 100, 50]), B.make_params(), "non-decreasing"),
+           (_batch([0, 100]), B.make_params(top_p=0.0), "top_p"),
+           (_batch([0, 100]), B.make_params(top_p=1.5), "top_p"),
+           (_batch([0, 100]), B.make_params(block=0), "block"),
+           (_batch([0, 16385 * 64]), B.make_params(), "blocks"),
+           (_batch([0, 100], Hq=4, Hkv=2, kv=[0, 0, 0, 1]), B.make_params(), "kv_of_q")]
+    for (bb, kk), p, word in bad:
+        with pytest.raises(B.UpfError) as e:
+            B.upf_workspace_bytes(bb, p)
+        assert word in e.value.message, (word, e.value.message)
+
+
+def test_workspace_size_is_device_independent(lib):
+    b, keep = _batch([0, 70000, 90000])
+    assert B.upf_workspace_bytes(b, B.make_params()) == B.upf_workspace_bytes(b, B.make_params())
+
+
+def test_calls_without_context_fail_before_launch(lib):
+    b, keep = _batch([0, 1000])
+    p = B.make_params()
+    with pytest.raises(B.UpfError) as e:
+        B.upf_score(None, b, p, 16, 4096, 16, 1024, 16, 256, 1 << 20)
+    assert e.value.status == 1 and "context" in e.value.message
+    io = B.make_compact_io(cu_seqlens_out=16, total_kept=16)
+    with pytest.raises(B.UpfError):
+        B.upf_compact(None, b, 16, io, 256, 1 << 20)
+    with pytest.raises(B.UpfError):
+        B.upf_select_tokens(None, b, p, 16, 4096, 16, 1024, 0, 0, 16, 16, io, 256, 1 << 20)
+
+
+def test_create_without_gpu_reports_an_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(B.UpfError) as e:
+        B.upf_create(0)
+    assert e.value.status in (1, 3)
+
+
+def test_destroy_null_is_an_argument_error(lib):
+    assert lib.upf_destroy(None) == 1
+    assert "NULL" in B.upf_last_error()

@@ -1,0 +1,331 @@
+"""GPU parity: libupf (through its C ABI) against the float64 oracle.
+
+Scores within 1e-3 relative (+1e-6/L absolute floor); the keep mask equal to
+the oracle's outside boundary blocks and exactly the top-p rule on the GPU's own
+block scores; compaction, metadata and drop history bit-exact given the mask.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import compare as C
+from sparse_long_context_tail_gb300 import _binding as B
+from sparse_long_context_tail_gb300 import workload as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sel():
+    import __graft_entry__
+    __graft_entry__.build()
+    from sparse_long_context_tail_gb300.selector import TokenSelector
+    s = TokenSelector(0)
+    yield s
+    s.close()
+
+
+DEV = torch.device("cuda", 0)
+
+
+def _up(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.to(DEV)
+
+
+def params_of(spec, **kw):
+    d = dict(n_tail=spec.n_tail, block=spec.block, sink_keep=spec.sink_keep, tail_keep=spec.tail_keep,
+             top_p=spec.top_p)
+    d.update(kw)
+    return B.make_params(**d)
+
+
+def run_gpu(sel, w, params, hidden=True, layer_id=5, history=None, history_len=None, kv_of_q=None):
+    s = w.spec
+    q = _up(w.q_full_bits().view(np.int16)).view(torch.bfloat16)
+    k = _up(w.k_bits.view(np.int16)).view(torch.bfloat16)
+    hid = _up(w.hidden_bits().view(np.int16)) if hidden else None
+    pos = _up(w.positions()) if hidden else None
+    slots = _up(w.slots()) if hidden else None
+    out = sel.select_tokens(q, k, w.cu_seqlens, _up(w.cu_seqlens), s.num_q_heads, s.num_kv_heads, s.head_dim,
+                            hid, pos, slots, layer_id=layer_id, history=history, history_len=history_len,
+                            params=params, kv_of_q=kv_of_q)
+    torch.cuda.synchronize()
+    status = sel.status()
+    return out, status, (hid, pos, slots)
+
+
+def ref_of(w, params, kv_of_q=None):
+    s = w.spec
+    scores = oracle.token_scores(w.k_bits, w.q_tail_bits, w.cu_seqlens, s.num_q_heads, s.num_kv_heads,
+                                 s.head_dim, params.n_tail, None, kv_of_q)
+    sel = oracle.select(scores, w.cu_seqlens, params.block, params.top_p, params.sink_keep, params.tail_keep)
+    return scores, sel
+
+
+def check(w, params, out, status, inputs, kv_of_q=None, check_hidden=True):
+    assert status == 0, B.STATUS_NAMES.get(status)
+    cu = w.cu_seqlens
+    T = w.total_tokens
+    scores, sel = ref_of(w, params, kv_of_q)
+    got = out.scores.cpu().numpy()
+    v = C.score_violations(got, scores, cu)
+    assert v["ok"], v
+    mask = C.unpack_bits(out.keep_bits.cpu().numpy(), T)
+    bad = C.mask_mismatches(mask, sel, cu, params.block, params.top_p, params.sink_keep, params.tail_keep)
+    assert not bad, bad[:10]
+    nb = TokenSelectorBlocks(cu, params.block)
+    bs = out.block_scores.cpu().numpy()[:nb]
+    bad2 = C.self_consistency_mismatches(mask, bs, cu, params.block, params.top_p, params.sink_keep,
+                                         params.tail_keep)
+    assert not bad2, bad2[:10]
+    # block scores against the oracle's block means of its own scores
+    ref_bs = np.concatenate([b for b in sel["block_scores"]]) if nb else np.zeros(0)
+    assert np.all(np.abs(bs - ref_bs) <= 1e-3 * np.abs(ref_bs) + 1e-6 / max(1, T)), "block means"
+    # compaction and metadata, bit-exact given the GPU's mask
+    comp = oracle.compact(mask, cu)
+    total = int(out.total_kept.item())
+    assert total == comp["total_kept"]
+    assert out.kept_count.cpu().numpy().tolist() == comp["kept_count"].tolist()
+    assert out.cu_seqlens_out.cpu().numpy().tolist() == comp["cu_seqlens_out"].tolist()
+    kidx = out.kept_index.cpu().numpy()[:total]
+    np.testing.assert_array_equal(kidx, comp["kept_index"])
+    hid, pos, slots = inputs
+    if hid is not None:
+        idx = torch.from_numpy(comp["kept_index"]).to(DEV)
+        np.testing.assert_array_equal(out.pos_out[:total].cpu().numpy(), w.positions()[comp["kept_index"]])
+        np.testing.assert_array_equal(out.slot_out[:total].cpu().numpy(), w.slots()[comp["kept_index"]])
+        if check_hidden:
+            assert torch.equal(out.hidden_out[:total], hid.index_select(0, idx))
+    return mask, sel
+
+
+def TokenSelectorBlocks(cu, G):
+    L = np.diff(np.asarray(cu, dtype=np.int64))
+    return int(sum(-(-int(x) // G) for x in L))
+
+
+# ----------------------------------------------------------- small cases ----
+
+SMALL = [
+    ("ragged-d64", dict(lengths=[1, 77, 300, 0, 1029, 4200], H=(4, 2, 64), hidden=512, n=128, G=64, planted=[0, 0, 1, 0, 3, 6])),
+    ("llama-2req", dict(lengths=[3000, 1700], H=(32, 8, 128), hidden=4096, n=128, G=64, planted=[4, 2])),
+    ("qwen-n512-G32", dict(lengths=[2500], H=(16, 2, 256), hidden=2048, n=512, G=32, planted=[5])),
+    ("gemma-n32-G128", dict(lengths=[2000, 640], H=(16, 8, 256), hidden=3840, n=32, G=128, planted=[2, 1])),
+    ("tail-only", dict(lengths=[100, 129, 257], H=(8, 2, 128), hidden=256, n=128, G=64, planted=[0, 0, 0])),
+    ("odd-hidden", dict(lengths=[3333], H=(8, 1, 128), hidden=520, n=64, G=16, planted=[7])),
+]
+
+
+def small_spec(name, c, seed=77):
+    Hq, Hkv, d = c["H"]
+    return wl.WorkloadSpec(name, c["lengths"], Hq, Hkv, d, c["hidden"], n_tail=c["n"], block=c["G"],
+                           planted=c["planted"], strength_range=(1.0, 4.0), seed=seed)
+
+
+@pytest.mark.parametrize("name,c", SMALL, ids=[s[0] for s in SMALL])
+def test_small_parity(sel, name, c):
+    spec = small_spec(name, c)
+    w = wl.generate(spec)
+    p = params_of(spec)
+    out, status, inputs = run_gpu(sel, w, p)
+    check(w, p, out, status, inputs)
+
+
+def test_explicit_kv_map(sel):
+    spec = wl.WorkloadSpec("kvmap", [1500, 900], 8, 2, 128, 256, planted=[2, 1], seed=5,
+                           kv_of_q=[0, 1, 0, 1, 0, 1, 0, 1])
+    w = wl.generate(spec)
+    p = params_of(spec)
+    out, status, inputs = run_gpu(sel, w, p, kv_of_q=spec.kv_of_q)
+    check(w, p, out, status, inputs, kv_of_q=spec.kv_of_q)
+
+
+def test_top_p_one_and_small_p(sel):
+    spec = small_spec("p1", SMALL[1][1])
+    w = wl.generate(spec)
+    for top_p in (1.0, 0.5):
+        p = params_of(spec, top_p=top_p)
+        out, status, inputs = run_gpu(sel, w, p)
+        check(w, p, out, status, inputs)
+
+
+def test_scale_parameter(sel):
+    spec = small_spec("scale", SMALL[0][1])
+    w = wl.generate(spec)
+    p = params_of(spec, softmax_scale=0.05)
+    out, status, inputs = run_gpu(sel, w, p, hidden=False)
+    s = w.spec
+    ref = oracle.token_scores(w.k_bits, w.q_tail_bits, w.cu_seqlens, s.num_q_heads, s.num_kv_heads, s.head_dim,
+                              s.n_tail, 0.05)
+    assert status == 0
+    assert C.score_violations(out.scores.cpu().numpy(), ref, w.cu_seqlens)["ok"]
+
+
+def test_entry_points_separately_match_fused(sel):
+    """upf_score, upf_select and upf_compact called one by one give the fused call's results."""
+    spec = small_spec("sep", SMALL[0][1])
+    w = wl.generate(spec)
+    p = params_of(spec)
+    fused, status, (hid, pos, slots) = run_gpu(sel, w, p)
+    s = w.spec
+    T = w.total_tokens
+    cu_dev = _up(w.cu_seqlens)
+    batch, keep = B.make_batch(cu_dev.data_ptr(), w.cu_seqlens, s.num_q_heads, s.num_kv_heads, s.head_dim)
+    nbytes = B.upf_workspace_bytes(batch, p)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    q = _up(w.q_full_bits().view(np.int16)).view(torch.bfloat16)
+    k = _up(w.k_bits.view(np.int16)).view(torch.bfloat16)
+    scores = torch.empty(T, dtype=torch.float32, device=DEV)
+    B.upf_score(sel.ctx, batch, p, q.data_ptr(), q.stride(0), k.data_ptr(), k.stride(0), scores.data_ptr(),
+                ws.data_ptr(), nbytes, torch.cuda.current_stream().cuda_stream)
+    bits = torch.empty((T + 31) // 32, dtype=torch.int32, device=DEV)
+    cnt = torch.empty(len(w.cu_seqlens) - 1, dtype=torch.int32, device=DEV)
+    B.upf_select(sel.ctx, batch, p, scores.data_ptr(), 0, bits.data_ptr(), cnt.data_ptr(), ws.data_ptr(), nbytes,
+                 torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert torch.equal(scores, fused.scores)
+    assert torch.equal(bits, fused.keep_bits)
+    assert torch.equal(cnt, fused.kept_count)
+
+
+def test_compact_with_oracle_mask(sel):
+    """Feed the oracle's mask to upf_compact: outputs and history are bit-exact."""
+    spec = small_spec("cmp", SMALL[0][1])
+    w = wl.generate(spec)
+    p = params_of(spec)
+    scores, ref = ref_of(w, p)
+    T, R = w.total_tokens, len(w.cu_seqlens) - 1
+    bits = _up(C.pack_bits(ref["mask"]).view(np.int32))
+    cu_dev = _up(w.cu_seqlens)
+    batch, keep = B.make_batch(cu_dev.data_ptr(), w.cu_seqlens, 1, 1, 64)
+    nbytes = B.upf_workspace_bytes(batch, B.make_params())
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    hid = _up(w.hidden_bits().view(np.int16))
+    pos, slots = _up(w.positions()), _up(w.slots())
+    hout, pout, sout = torch.empty_like(hid), torch.empty_like(pos), torch.empty_like(slots)
+    kidx = torch.empty(T, dtype=torch.int32, device=DEV)
+    cuo = torch.empty(R + 1, dtype=torch.int32, device=DEV)
+    tot = torch.empty(1, dtype=torch.int32, device=DEV)
+    cap = 3
+    hist0 = np.zeros((R, cap, 2), dtype=np.int32)
+    hist0[:, 0] = [[1, 11]] * R
+    hlen0 = np.ones(R, dtype=np.int32)
+    hist, hlen = _up(hist0), _up(hlen0)
+    io = B.make_compact_io(hid.stride(0) * 2, hid.data_ptr(), hout.data_ptr(), pos.data_ptr(), pout.data_ptr(),
+                           slots.data_ptr(), sout.data_ptr(), kidx.data_ptr(), cuo.data_ptr(), tot.data_ptr(), 9,
+                           cap, hist.data_ptr(), hlen.data_ptr())
+    stream = torch.cuda.current_stream().cuda_stream
+    B.upf_compact(sel.ctx, batch, bits.data_ptr(), io, ws.data_ptr(), nbytes, stream)
+    torch.cuda.synchronize()
+    assert sel.status() == 0
+    comp = oracle.compact(ref["mask"], w.cu_seqlens, w.hidden_bits(), w.positions(), w.slots(), 9, hist0, hlen0)
+    total = comp["total_kept"]
+    assert int(tot.item()) == total
+    np.testing.assert_array_equal(kidx[:total].cpu().numpy(), comp["kept_index"])
+    np.testing.assert_array_equal(cuo.cpu().numpy(), comp["cu_seqlens_out"])
+    np.testing.assert_array_equal(hout[:total].cpu().numpy().view(np.uint16), comp["hidden_out"])
+    np.testing.assert_array_equal(pout[:total].cpu().numpy(), comp["positions_out"])
+    np.testing.assert_array_equal(sout[:total].cpu().numpy(), comp["slots_out"])
+    np.testing.assert_array_equal(hist.cpu().numpy(), comp["history"])
+    np.testing.assert_array_equal(hlen.cpu().numpy(), comp["history_len"])
+    # fill the history to capacity, then one more call must report CAPACITY and write nothing
+    B.upf_compact(sel.ctx, batch, bits.data_ptr(), io, ws.data_ptr(), nbytes, stream)
+    torch.cuda.synchronize()
+    assert sel.status() == 0
+    before = hist.clone(), hlen.clone()
+    B.upf_compact(sel.ctx, batch, bits.data_ptr(), io, ws.data_ptr(), nbytes, stream)
+    torch.cuda.synchronize()
+    assert sel.status() == 4
+    assert torch.equal(hist, before[0]) and torch.equal(hlen, before[1])
+    assert sel.status() == 0   # the status word was cleared by the read
+
+
+def test_compact_all_and_none(sel):
+    T = 5000
+    cu = np.array([0, 1234, 1234, 5000], dtype=np.int32)
+    cu_dev = _up(cu)
+    batch, keep = B.make_batch(cu_dev.data_ptr(), cu, 1, 1, 64)
+    nbytes = B.upf_workspace_bytes(batch, B.make_params())
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    hid = torch.randint(-30000, 30000, (T, 24), dtype=torch.int16, device=DEV)
+    for fill in (0, -1):
+        bits = torch.full(((T + 31) // 32,), fill, dtype=torch.int32, device=DEV)
+        hout = torch.zeros_like(hid)
+        kidx = torch.empty(T, dtype=torch.int32, device=DEV)
+        cuo = torch.empty(4, dtype=torch.int32, device=DEV)
+        tot = torch.empty(1, dtype=torch.int32, device=DEV)
+        io = B.make_compact_io(48, hid.data_ptr(), hout.data_ptr(), kept_index=kidx.data_ptr(),
+                               cu_seqlens_out=cuo.data_ptr(), total_kept=tot.data_ptr())
+        B.upf_compact(sel.ctx, batch, bits.data_ptr(), io, ws.data_ptr(), nbytes, torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        n = int(tot.item())
+        if fill == 0:
+            assert n == 0 and cuo.cpu().tolist() == [0, 0, 0, 0]
+        else:   # all bits set, including stray bits past T in the last word
+            assert n == T and cuo.cpu().tolist() == cu.tolist()
+            assert torch.equal(hout, hid) and torch.equal(kidx.cpu(), torch.arange(T, dtype=torch.int32))
+
+
+def test_nonfinite_scores_are_reported(sel):
+    cu = np.array([0, 640, 1000], dtype=np.int32)
+    T = 1000
+    cu_dev = _up(cu)
+    batch, keep = B.make_batch(cu_dev.data_ptr(), cu, 1, 1, 64)
+    p = B.make_params()
+    nbytes = B.upf_workspace_bytes(batch, p)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    scores = torch.full((T,), 1.0 / 640, device=DEV)
+    scores[700] = float("nan")
+    bits = torch.empty((T + 31) // 32, dtype=torch.int32, device=DEV)
+    cnt = torch.empty(2, dtype=torch.int32, device=DEV)
+    B.upf_select(sel.ctx, batch, p, scores.data_ptr(), 0, bits.data_ptr(), cnt.data_ptr(), ws.data_ptr(), nbytes,
+                 torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert sel.status() == 5
+    assert cnt.cpu().tolist()[1] == 360      # the request with the NaN keeps everything
+
+
+def test_inconsistent_device_cu_seqlens_is_reported(sel):
+    cu_host = np.array([0, 500, 1000], dtype=np.int32)
+    cu_dev = _up(np.array([0, 700, 900], dtype=np.int32))    # device copy disagrees on the total
+    batch, keep = B.make_batch(cu_dev.data_ptr(), cu_host, 1, 1, 64)
+    p = B.make_params()
+    nbytes = B.upf_workspace_bytes(batch, p)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    scores = torch.full((1000,), 1e-3, device=DEV)
+    bits = torch.empty(32, dtype=torch.int32, device=DEV)
+    cnt = torch.empty(2, dtype=torch.int32, device=DEV)
+    B.upf_select(sel.ctx, batch, p, scores.data_ptr(), 0, bits.data_ptr(), cnt.data_ptr(), ws.data_ptr(), nbytes,
+                 torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert sel.status() == 1
+
+
+def test_repeat_calls_are_deterministic(sel):
+    spec = small_spec("det", SMALL[1][1])
+    w = wl.generate(spec)
+    p = params_of(spec)
+    a, _, _ = run_gpu(sel, w, p, hidden=False)
+    sa, ba = a.scores.clone(), a.keep_bits.clone()
+    b, _, _ = run_gpu(sel, w, p, hidden=False)
+    assert torch.equal(sa, b.scores) and torch.equal(ba, b.keep_bits)
+
+
+# ----------------------------------------------- the benchmark workloads ----
+
+FULL = ["small-L4096", "llama8b-L32768", "llama8b-L131072", "llama8b-batch16",
+        "qwen3next-G64-n128", "gemma3-G64-n128", "qwen3next-G32-n512", "gemma3-G128-n32",
+        "qwen3next-G128-n32", "gemma3-G32-n512"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload(sel, name):
+    spec = wl.named_spec(name)
+    w = wl.generate(spec)
+    p = params_of(spec)
+    out, status, inputs = run_gpu(sel, w, p)
+    check(w, p, out, status, inputs)
