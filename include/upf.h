@@ -213,6 +213,35 @@ upf_status upf_select_tokens(upf_ctx* ctx, const upf_batch* batch, const upf_par
                              float* scores, float* block_scores, uint32_t* keep_bits, int32_t* kept_count,
                              const upf_compact_io* io, void* ws, size_t ws_bytes, void* stream);
 
+/* No-allocation variant of upf_select.  The article has no counterpart: this
+ * is an integration entry point for callers that cannot allocate device
+ * memory -- a serving engine that reserves nearly all GPU memory for its own
+ * pools at start-up and gives libraries no allocation hook, or a plugin that
+ * runs inside such an engine and may not bypass its allocator.  It needs no
+ * context and no workspace: the scratch of the select kernels (the batch
+ * descriptor and, if block_scores is NULL, the block means) lives in one
+ * fixed-size device array compiled into the library, about 270 KiB, which
+ * every GPU that loads the library holds until the process exits.
+ * It runs on the caller's current device and stream.
+ * Same inputs, outputs and results as upf_select.  Limits: at most
+ * UPF_NOALLOC_MAX_REQS requests and UPF_NOALLOC_MAX_BLOCKS blocks in total
+ * (and 16384 per request); larger batches return UPF_ERR_UNSUPPORTED.
+ * status_dev: device int32 [1] (nullable) that receives device-detected
+ * errors (first error wins; the caller clears it); when NULL such errors go to
+ * a status word inside the array and are not reported.
+ * The array is shared by every call and keeps the last call's contents; each
+ * call rewrites what it reads.  Calls whose GPU work overlaps (different
+ * streams or host threads) race on it: serialise them.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture begins.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.  Errors:
+ * INVALID_ARG, UNSUPPORTED, CUDA (message in upf_last_error()). */
+#define UPF_NOALLOC_MAX_REQS 1024
+#define UPF_NOALLOC_MAX_BLOCKS 65536
+upf_status upf_select_noalloc(const upf_batch* batch, const upf_params* params, const float* scores,
+                              float* block_scores, uint32_t* keep_bits, int32_t* kept_count,
+                              int32_t* status_dev, void* stream);
+
 /* Tracing (per-stage device timing).  Stages, in launch order:
  * 0 describe (batch descriptor), 1 score pass 1, 2 score pass 2, 3 finalize /
  * block means, 4 select, 5 compact count, 6 compact index, 7 compact gather. */

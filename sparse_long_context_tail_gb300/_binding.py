@@ -62,6 +62,8 @@ _SIGNATURES = {
                     c_void_p, c_size_t, c_void_p], c_int),
     "upf_compact": ([c_void_p, POINTER(UpfBatch), c_void_p, POINTER(UpfCompactIO), c_void_p, c_size_t, c_void_p],
                     c_int),
+    "upf_select_noalloc": ([POINTER(UpfBatch), POINTER(UpfParams), c_void_p, c_void_p, c_void_p, c_void_p,
+                            c_void_p, c_void_p], c_int),
     "upf_stage_name": ([c_int32], c_char_p),
     "upf_profile_enable": ([c_void_p, c_int32], c_int),
     "upf_profile_read": ([c_void_p, c_void_p, c_void_p, c_int32], c_int),
@@ -173,6 +175,12 @@ def upf_score(ctx, batch, params, q, q_row_stride, k, k_row_stride, scores, ws, 
 def upf_select(ctx, batch, params, scores, block_scores, keep_bits, kept_count, ws, ws_bytes, stream=0):
     _check(load().upf_select(ctx, ctypes.byref(batch), ctypes.byref(params), scores, block_scores or None,
                              keep_bits, kept_count, ws, ws_bytes, stream or None))
+
+
+def upf_select_noalloc(batch, params, scores, block_scores, keep_bits, kept_count, status_dev=0, stream=0):
+    """upf_select without a context or workspace (scratch in a fixed array inside the library)."""
+    _check(load().upf_select_noalloc(ctypes.byref(batch), ctypes.byref(params), scores, block_scores or None,
+                                     keep_bits, kept_count, status_dev or None, stream or None))
 
 
 def upf_compact(ctx, batch, keep_bits, io: UpfCompactIO, ws, ws_bytes, stream=0):

@@ -403,6 +403,8 @@ upf_status launch_compact_all(upf_ctx* ctx, const upf::CompactArgs& ca, cudaStre
 
 }  // namespace
 
+void upf::set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
 extern "C" {
 
 int upf_version(void) { return UPF_VERSION; }

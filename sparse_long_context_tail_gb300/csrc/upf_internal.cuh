@@ -101,6 +101,9 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// Sets the thread-local message returned by upf_last_error().
+void set_last_error(const char* msg);
+
 // Launchers (defined in the kernel translation units); all return cudaGetLastError().
 cudaError_t launch_describe(const DescribeArgs& a, cudaStream_t s);
 cudaError_t launch_score_pass1(const ScoreArgs& a, cudaStream_t s);
