@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 STAGES = ["describe", "score_pass1", "score_pass2", "finalize", "select", "compact_count", "compact_index",
           "compact_gather"]
 # kernel sources per stage (for the traffic record's freshness check)
-STAGE_SOURCES = {"score_pass1": "score_simt.cu", "score_pass2": "score_simt.cu", "finalize": "select.cu",
+STAGE_SOURCES = {"score_pass1": "score_tc.cu", "score_pass2": "score_tc.cu", "finalize": "select.cu",
                  "select": "select.cu", "compact_gather": "compact.cu", "compact_index": "compact.cu",
                  "compact_count": "compact.cu", "describe": "score_simt.cu"}
 
@@ -121,6 +121,32 @@ def traffic_record(stage, workload):
     except (OSError, ValueError, KeyError):
         return None
     return None
+
+
+# ------------------------------------------------------------- multi-GPU ----
+
+def rank_spec(spec, rank):
+    """The requests rank `rank` processes: the same workload shape with its own seed.
+
+    Requests are independent, so N GPUs each take their own batch (weak
+    scaling) and exchange nothing on the data path."""
+    import dataclasses
+    return spec if rank == 0 else dataclasses.replace(spec, seed=spec.seed + 100 * rank)
+
+
+def aggregate_over_ranks(seconds_per_step, tokens, dist_mod=None, device=None):
+    """Whole-job rate: units of all ranks / the slowest rank's step time.
+
+    Returns (max seconds per step, total tokens per step, tokens/s)."""
+    if dist_mod is not None and dist_mod.is_available() and dist_mod.is_initialized() and \
+            dist_mod.get_world_size() > 1:
+        import torch
+        t = torch.tensor([float(seconds_per_step)], dtype=torch.float64, device=device)
+        n = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+        dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+        dist_mod.all_reduce(n, op=dist_mod.ReduceOp.SUM)
+        seconds_per_step, tokens = float(t.item()), float(n.item())
+    return seconds_per_step, tokens, tokens / seconds_per_step
 
 
 # ----------------------------------------------------------------- clocks ----
@@ -284,7 +310,7 @@ def main():
     from sparse_long_context_tail_gb300 import _binding as B
     from sparse_long_context_tail_gb300.selector import TokenSelector
 
-    spec = wl.named_spec(args.workload)
+    spec = rank_spec(wl.named_spec(args.workload), rank)
     if args.top_p is not None:
         spec.top_p = args.top_p
     t0 = time.time()
@@ -348,12 +374,8 @@ def main():
     B.upf_profile_enable(sel.ctx, False)
     clk = clocks.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * T / (ms / 1e3)
+    sec, _, value = aggregate_over_ranks(statistics.mean(step_ms) / 1e3, T, dist if world > 1 else None, dev)
+    ms = sec * 1e3
 
     # roofline of the dominant kernel (largest share of device time)
     work = algorithmic_work(spec, cu, kept_total, hid_dev.stride(0) * 2, spec.top_p)
@@ -463,13 +485,9 @@ def run_e2e(args, torch, sel, spec, w, cu, params, q_dev, k_dev, hid_dev, pos_de
             times.append(dt)
             d2h_total = 4 + bits_h.numel() * 4 + cnt_h.numel() * 4 + cuo_h.numel() * 4 + \
                 total * (hid_dev.stride(0) * 2 + 16)
-    per = statistics.mean(times)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([per], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        per = float(t.item())
-    return {"value": world * T / per, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h_total),
+    import torch.distributed as dist
+    per, _, rate = aggregate_over_ranks(statistics.mean(times), T, dist if world > 1 else None, dev)
+    return {"value": rate, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h_total),
             "ms_per_step": per * 1e3, "steps": len(times),
             "note": "wall clock around pinned H2D of the step's inputs (K, tail Q rows, hidden, positions, slots, "
                     "cu_seqlens), the call, and D2H of the mask, counts, offsets and the kept rows"}

@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -79,6 +80,8 @@ struct Plan {
   int n = 0, G = 0, sink = 0, tail = 0;
   float top_p = 0.f, scale = 0.f;
   int QR = 0, QC = 0, NQC = 0, KS1 = 0, KS2 = 0;
+  int q_box_rows = 0;
+  bool use_tc = false;
   long long items1 = 0, items2 = 0;
   long long NB = 0;
   int max_nb = 0;
@@ -169,9 +172,23 @@ upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p
     pl->top_p = p->top_p;
     pl->scale = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / std::sqrt(float(b->head_dim));
     pl->QR = pl->gamma * pl->n;
-    const int qc_max = 512;
-    pl->QC = std::min(pl->QR, qc_max);
+    // Query rows per chunk: the whole group's tail rows when they fit the
+    // tensor-core kernels' shared-memory budget (512 rows of d <= 128, 256 rows
+    // of d = 256), rounded up to whole 128-row MMA tiles.
+    const int qc_max = pl->d <= 128 ? 512 : 256;
+    pl->QC = std::min(((pl->QR + 127) / 128) * 128, qc_max);
     pl->NQC = ceil_div(pl->QR, pl->QC);
+    // Tensor-core kernels load tail rows in TMA boxes of 16..128 rows that
+    // divide n; other n fall back to the CUDA-core kernels.  UPF_SCORE_PATH=simt
+    // forces the CUDA-core kernels (used by tests to cross-check the two).
+    pl->q_box_rows = 0;
+    for (int rows = 128; rows >= 16; rows >>= 1)
+      if (pl->n % rows == 0) {
+        pl->q_box_rows = rows;
+        break;
+      }
+    const char* path = std::getenv("UPF_SCORE_PATH");
+    pl->use_tc = pl->q_box_rows > 0 && !(path && std::strcmp(path, "simt") == 0);
     // The split depends only on the batch and parameters (never on the device),
     // so upf_workspace_bytes() without a context sizes exactly what a call uses.
     (void)ctx;
@@ -288,6 +305,8 @@ upf::ScoreArgs score_args(const upf_ctx* ctx, const upf_batch* b, const Plan& pl
   a.items1 = int(pl.items1);
   a.items2 = int(pl.items2);
   a.scale_log2 = pl.scale * 1.4426950408889634f;
+  a.q_box_rows = pl.q_box_rows;
+  a.use_tc = pl.use_tc ? 1 : 0;
   a.item_off1 = at<int32_t>(ws, pl.off_desc);
   a.item_off2 = at<int32_t>(ws, pl.off_desc) + (pl.R + 1);
   a.p1part = at<float2>(ws, pl.off_p1);

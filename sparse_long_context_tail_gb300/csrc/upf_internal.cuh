@@ -39,6 +39,8 @@ struct ScoreArgs {
   int32_t KS1, KS2;
   int32_t items1, items2;  // host totals (grid sizes)
   float scale_log2;
+  int32_t q_box_rows;        // tail rows per TMA box of q (divides n)
+  int32_t use_tc;            // 1: tcgen05 kernels, 0: CUDA-core kernels
   const int32_t* item_off1;  // [R+1]
   const int32_t* item_off2;  // [R+1]
   float2* p1part;            // [items1][QC]
@@ -108,6 +110,9 @@ void set_last_error(const char* msg);
 cudaError_t launch_describe(const DescribeArgs& a, cudaStream_t s);
 cudaError_t launch_score_pass1(const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_score_pass2(const ScoreArgs& a, cudaStream_t s);
+cudaError_t launch_score_pass1_tc(const ScoreArgs& a, cudaStream_t s);
+cudaError_t launch_score_pass2_tc(const ScoreArgs& a, cudaStream_t s);
+size_t score_tc_smem_bytes(int d, int QC);
 cudaError_t launch_block_means(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_compact_count(const CompactArgs& a, cudaStream_t s);

@@ -135,6 +135,26 @@ def test_small_parity(sel, name, c):
     check(w, p, out, status, inputs)
 
 
+@pytest.mark.parametrize("name,c", [SMALL[0], SMALL[2]], ids=["ragged-d64", "qwen-n512-G32"])
+def test_cuda_core_fallback_parity(sel, name, c, monkeypatch):
+    """The CUDA-core scoring kernels (used when n is not a multiple of 16) against the oracle."""
+    monkeypatch.setenv("UPF_SCORE_PATH", "simt")
+    spec = small_spec(name, c)
+    w = wl.generate(spec)
+    p = params_of(spec)
+    out, status, inputs = run_gpu(sel, w, p)
+    check(w, p, out, status, inputs)
+
+
+def test_odd_tail_count_uses_fallback(sel):
+    """n = 100 (not a multiple of 16) runs on the CUDA-core kernels."""
+    spec = wl.WorkloadSpec("n100", [900, 2048], 8, 2, 128, 256, n_tail=100, block=64, planted=[1, 2], seed=9)
+    w = wl.generate(spec)
+    p = params_of(spec)
+    out, status, inputs = run_gpu(sel, w, p)
+    check(w, p, out, status, inputs)
+
+
 def test_explicit_kv_map(sel):
     spec = wl.WorkloadSpec("kvmap", [1500, 900], 8, 2, 128, 256, planted=[2, 1], seed=5,
                            kv_of_q=[0, 1, 0, 1, 0, 1, 0, 1])
