@@ -358,7 +358,8 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     B.upf_profile_read(sel.ctx)          # reset counters
-    B.upf_profile_enable(sel.ctx, True)
+    # Headline loop: tracing off, so consecutive kernels of a step overlap
+    # their launch with the predecessor's tail (programmatic dependent launch).
     wall0 = time.perf_counter()
     for i in range(args.steps):
         starts[i].record(stream)
@@ -368,12 +369,24 @@ def main():
             flush.zero_()
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    launches, _ = B.upf_profile_read(sel.ctx)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    # Breakdown loop: the same steps with an event pair around every launch.
+    B.upf_profile_enable(sel.ctx, True)
+    traced = []
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        if flush is not None:
+            flush.zero_()
+    torch.cuda.synchronize()
+    traced = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    _, stage_ms = B.upf_profile_read(sel.ctx)
+    B.upf_profile_enable(sel.ctx, False)
     if world > 1:
         dist.barrier()
-    launches, stage_ms = B.upf_profile_read(sel.ctx)
-    B.upf_profile_enable(sel.ctx, False)
     clk = clocks.stop()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     sec, _, value = aggregate_over_ranks(statistics.mean(step_ms) / 1e3, T, dist if world > 1 else None, dev)
     ms = sec * 1e3
 
@@ -428,7 +441,8 @@ def main():
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded bf16 N(0,1) + planted blocks)",
                 "config": config_of(spec, w, args),
-                "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
+                "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms),
+                            "traced_mean": statistics.mean(traced), "stage_sum": sum(stage_ms) / args.steps},
                 "kept_tokens": kept_total, "kept_fraction": kept_total / T,
                 "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": int(sum(launches)), "clocks": clk, "wall_s": wall}

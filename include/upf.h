@@ -187,8 +187,9 @@ upf_status upf_score(upf_ctx* ctx, const upf_batch* batch, const upf_params* par
  * keep_bits:    device uint32 [ceil(T/32)]: bit (t % 32) of word t/32 is 1 iff
  *               packed token t is kept.  Bits past T are 0.
  * kept_count:   device int32 [R]: kept tokens per request.
- * A request with more than 16384 blocks is UNSUPPORTED.  A NaN/Inf block score
- * sets UPF_ERR_NONFINITE in the status word and keeps that whole request.
+ * A request with more than 16384 blocks is UNSUPPORTED.  Scores are importances
+ * (probabilities): a NaN, infinite or negative block score sets
+ * UPF_ERR_NONFINITE in the status word and keeps that whole request.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 upf_status upf_select(upf_ctx* ctx, const upf_batch* batch, const upf_params* params,
                       const float* scores, float* block_scores, uint32_t* keep_bits,
@@ -212,6 +213,31 @@ upf_status upf_select_tokens(upf_ctx* ctx, const upf_batch* batch, const upf_par
                              const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
                              float* scores, float* block_scores, uint32_t* keep_bits, int32_t* kept_count,
                              const upf_compact_io* io, void* ws, size_t ws_bytes, void* stream);
+
+/* Revival of frozen tokens (section 二, third step: the hidden states of
+ * dropped tokens are frozen and carried forward so they can be revived).
+ * Writes the rows a compacted batch produced back to their token positions
+ * in the full-length buffer: full[kept_index[o]] = rows[o] for o < *total_kept;
+ * rows of dropped tokens in `full` keep their frozen contents.
+ * kept_index, total_kept: device int32 [T] / [1] as written by upf_compact.
+ * rows: device [>= total_kept, row_bytes]; full: device [T, row_bytes] with
+ * T = batch cu_seqlens_host[R]; row_bytes a positive multiple of 16, both
+ * pointers 16-byte aligned.  Indices outside [0, T) are skipped.
+ * Errors: INVALID_ARG, CUDA. */
+upf_status upf_revive(upf_ctx* ctx, const upf_batch* batch, const int32_t* kept_index, const int32_t* total_kept,
+                      const void* rows, int64_t row_bytes, void* full, void* stream);
+
+/* KV entries each request's layer `layer_id` holds (section 三, last
+ * paragraph: decode reads the drop-history bill to know how many KV entries
+ * each layer wrote).  A drop at full-attention layer l keeps c tokens for that
+ * layer and every later one until the next drop, so kv_len[r] = c of the
+ * latest record of request r whose layer id <= layer_id (records are appended
+ * in layer order), or the prompt length L_r if there is none.
+ * history, history_len, history_cap: as in upf_compact_io (device).
+ * kv_len: device int32 [R].  Errors: INVALID_ARG, CUDA. */
+upf_status upf_history_kv_len(upf_ctx* ctx, const upf_batch* batch, const int32_t* history,
+                              const int32_t* history_len, int32_t history_cap, int32_t layer_id, int32_t* kv_len,
+                              void* stream);
 
 /* No-allocation variant of upf_select.  The article has no counterpart: this
  * is an integration entry point for callers that cannot allocate device

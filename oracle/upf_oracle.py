@@ -285,6 +285,38 @@ def compact(mask: np.ndarray, cu_seqlens: Sequence[int], hidden: Optional[np.nda
     return out
 
 
+def revive(full: np.ndarray, kept_index: np.ndarray, rows: np.ndarray) -> np.ndarray:
+    """Write a compacted batch's rows back into the full-length buffer [§2 step 3].
+
+    Dropped tokens keep their frozen hidden states; kept token kept_index[o]
+    takes row o of the compacted batch.  Returns an updated copy of `full`.
+    """
+    out = np.array(full, copy=True)
+    out[np.asarray(kept_index, dtype=np.int64)] = rows
+    return out
+
+
+def history_kv_len(history: np.ndarray, history_len: np.ndarray, cu_seqlens: Sequence[int], layer_id: int) -> np.ndarray:
+    """KV entries each request's layer `layer_id` holds, read from the drop history [§3 history].
+
+    A drop at full-attention layer l_i keeps c_i tokens; that layer and every
+    later one up to the next drop process (and cache) only those tokens, so
+    layer `layer_id` holds c_i of the latest record with l_i <= layer_id, and
+    the prompt length L_r when no drop happened at or before it.  Records are
+    in append order (non-decreasing layer ids).
+    """
+    cu = [int(x) for x in cu_seqlens]
+    R = len(cu) - 1
+    out = np.zeros(R, dtype=np.int64)
+    for r in range(R):
+        kv = cu[r + 1] - cu[r]
+        for i in range(int(history_len[r])):
+            if int(history[r][i][0]) <= layer_id:
+                kv = int(history[r][i][1])
+        out[r] = kv
+    return out
+
+
 def select_tokens(k_bits, q_tail_bits, cu_seqlens, num_q_heads, num_kv_heads, head_dim, n_tail=128,
                   block=64, top_p=0.99, sink_keep=128, tail_keep=128, softmax_scale=None, kv_of_q=None,
                   hidden=None, positions=None, slots=None, layer_id=0, history=None, history_len=None,

@@ -64,6 +64,9 @@ _SIGNATURES = {
                     c_int),
     "upf_select_noalloc": ([POINTER(UpfBatch), POINTER(UpfParams), c_void_p, c_void_p, c_void_p, c_void_p,
                             c_void_p, c_void_p], c_int),
+    "upf_revive": ([c_void_p, POINTER(UpfBatch), c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p], c_int),
+    "upf_history_kv_len": ([c_void_p, POINTER(UpfBatch), c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p],
+                           c_int),
     "upf_stage_name": ([c_int32], c_char_p),
     "upf_profile_enable": ([c_void_p, c_int32], c_int),
     "upf_profile_read": ([c_void_p, c_void_p, c_void_p, c_int32], c_int),
@@ -185,6 +188,15 @@ def upf_select_noalloc(batch, params, scores, block_scores, keep_bits, kept_coun
 
 def upf_compact(ctx, batch, keep_bits, io: UpfCompactIO, ws, ws_bytes, stream=0):
     _check(load().upf_compact(ctx, ctypes.byref(batch), keep_bits, ctypes.byref(io), ws, ws_bytes, stream or None))
+
+
+def upf_revive(ctx, batch, kept_index, total_kept, rows, row_bytes, full, stream=0):
+    _check(load().upf_revive(ctx, ctypes.byref(batch), kept_index, total_kept, rows, row_bytes, full, stream or None))
+
+
+def upf_history_kv_len(ctx, batch, history, history_len, history_cap, layer_id, kv_len, stream=0):
+    _check(load().upf_history_kv_len(ctx, ctypes.byref(batch), history, history_len, history_cap, layer_id, kv_len,
+                                     stream or None))
 
 
 NUM_STAGES = 8

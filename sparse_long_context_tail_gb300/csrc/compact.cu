@@ -42,6 +42,8 @@ __device__ __forceinline__ int block_sum(int v, int* s_tmp) {
 }
 
 __global__ void __launch_bounds__(kChunkThreads) compact_count_kernel(const CompactArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int s_tmp[kChunkThreads / 32];
   const int c = blockIdx.x;
   int cnt = 0;
@@ -54,6 +56,8 @@ __global__ void __launch_bounds__(kChunkThreads) compact_count_kernel(const Comp
 }
 
 __global__ void __launch_bounds__(kChunkThreads) compact_index_kernel(const CompactArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int s_tmp[kChunkThreads / 32];
   __shared__ int s_woff[kCompactChunkWords + 1];  // exclusive kept-token prefix per word of the chunk
   __shared__ int s_warp[kChunkThreads / 32];
@@ -124,6 +128,8 @@ __global__ void __launch_bounds__(kChunkThreads) compact_index_kernel(const Comp
 }
 
 __global__ void __launch_bounds__(256) compact_gather_kernel(const CompactArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int total = min(*a.total_kept, a.T);
   // Drop history: one record per request, all or nothing.
   if (blockIdx.x == 0 && threadIdx.x == 0 && a.history) {
@@ -167,24 +173,21 @@ __global__ void __launch_bounds__(256) compact_gather_kernel(const CompactArgs a
 
 }  // namespace
 
-cudaError_t launch_compact_count(const CompactArgs& a, cudaStream_t s) {
-  compact_count_kernel<<<a.nchunks, kChunkThreads, 0, s>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_compact_count(const CompactArgs& a, cudaStream_t s, bool pdl) {
+  return launch_kernel(compact_count_kernel, a.nchunks, kChunkThreads, 0, s, pdl, a);
 }
 
-cudaError_t launch_compact_index(const CompactArgs& a, cudaStream_t s) {
-  compact_index_kernel<<<a.nchunks, kChunkThreads, 0, s>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_compact_index(const CompactArgs& a, cudaStream_t s, bool pdl) {
+  return launch_kernel(compact_index_kernel, a.nchunks, kChunkThreads, 0, s, pdl, a);
 }
 
-cudaError_t launch_compact_gather(const CompactArgs& a, cudaStream_t s) {
+cudaError_t launch_compact_gather(const CompactArgs& a, cudaStream_t s, bool pdl) {
   // Enough warps to cover every row in one pass when few rows survive, capped
   // at a few waves of resident warps.
   int blocks = (a.T + 7) / 8;
   blocks = blocks < 1 ? 1 : blocks;
   blocks = blocks > 8 * kPlanSMs ? 8 * kPlanSMs : blocks;
-  compact_gather_kernel<<<blocks, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(compact_gather_kernel, blocks, 256, 0, s, pdl, a);
 }
 
 }  // namespace upf

@@ -45,60 +45,52 @@ __device__ __forceinline__ Item locate(const int32_t* item_off, const int32_t* c
   return it;
 }
 
-__global__ void describe_kernel(const DescribeArgs a) {
-  __shared__ int s_scan[3][1024];
-  __shared__ int s_carry[3];
-  __shared__ int s_bad;
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    s_carry[0] = s_carry[1] = s_carry[2] = 0;
-    s_bad = (a.cu[0] != 0 || a.cu[a.R] != a.T) ? 1 : 0;
-  }
-  __syncthreads();
-  for (int base = 0; base < a.R; base += blockDim.x) {
-    const int r = base + tid;
+// One warp: per-request item counts of both passes and block counts, scanned
+// 32 requests at a time with shuffles.
+__global__ void __launch_bounds__(32) describe_kernel(const DescribeArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x;
+  bool bad = lane == 0 && (a.cu[0] != 0 || a.cu[a.R] != a.T);
+  int carry[3] = {0, 0, 0};
+  for (int base = 0; base < a.R; base += 32) {
+    const int r = base + lane;
     int v[3] = {0, 0, 0};
     if (r < a.R) {
       const int L = a.cu[r + 1] - a.cu[r];
-      if (L < 0) atomicExch(&s_bad, 1);
+      bad |= L < 0;
       const int Lc = L < 0 ? 0 : L;
       v[0] = a.Hkv * a.NQC * ceil_div_dev(Lc, a.KS1);
       v[1] = a.Hkv * a.NQC * ceil_div_dev(Lc, a.KS2);
       v[2] = ceil_div_dev(Lc, a.G);
     }
-    for (int c = 0; c < 3; ++c) s_scan[c][tid] = v[c];
-    __syncthreads();
-    // Hillis-Steele inclusive scan over the chunk (sizes are small).
-    for (int off = 1; off < blockDim.x; off <<= 1) {
-      int t[3];
-      for (int c = 0; c < 3; ++c) t[c] = tid >= off ? s_scan[c][tid - off] : 0;
-      __syncthreads();
-      for (int c = 0; c < 3; ++c) s_scan[c][tid] += t[c];
-      __syncthreads();
-    }
+    int incl[3] = {v[0], v[1], v[2]};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+      for (int c = 0; c < 3; ++c) {
+        const int t = __shfl_up_sync(0xffffffffu, incl[c], o);
+        if (lane >= o) incl[c] += t;
+      }
     if (r < a.R) {
-      a.item_off1[r] = s_carry[0] + s_scan[0][tid] - v[0];
-      a.item_off2[r] = s_carry[1] + s_scan[1][tid] - v[1];
-      a.blk_off[r] = s_carry[2] + s_scan[2][tid] - v[2];
+      a.item_off1[r] = carry[0] + incl[0] - v[0];
+      a.item_off2[r] = carry[1] + incl[1] - v[1];
+      a.blk_off[r] = carry[2] + incl[2] - v[2];
     }
-    __syncthreads();
-    if (tid == blockDim.x - 1)
-      for (int c = 0; c < 3; ++c) s_carry[c] += s_scan[c][tid];
-    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < 3; ++c) carry[c] += __shfl_sync(0xffffffffu, incl[c], 31);
   }
-  if (tid == 0) {
-    a.item_off1[a.R] = s_carry[0];
-    a.item_off2[a.R] = s_carry[1];
-    a.blk_off[a.R] = s_carry[2];
-  }
-  __syncthreads();
   // The grids were sized on the host from cu_seqlens_host; a device copy that
   // disagrees must not drive any work.
-  if (tid == 0 && (s_carry[0] != a.items1 || s_carry[1] != a.items2 || s_carry[2] != a.NB)) s_bad = 1;
-  __syncthreads();
-  if (s_bad) {
-    for (int r = tid; r <= a.R; r += blockDim.x) a.item_off1[r] = a.item_off2[r] = a.blk_off[r] = 0;
-    if (tid == 0) set_status(a.status, UPF_ERR_INVALID_ARG);
+  bad |= carry[0] != a.items1 || carry[1] != a.items2 || carry[2] != a.NB;
+  bad = __any_sync(0xffffffffu, bad);
+  if (bad) {
+    for (int r = lane; r <= a.R; r += 32) a.item_off1[r] = a.item_off2[r] = a.blk_off[r] = 0;
+    if (lane == 0) set_status(a.status, UPF_ERR_INVALID_ARG);
+  } else if (lane == 0) {
+    a.item_off1[a.R] = carry[0];
+    a.item_off2[a.R] = carry[1];
+    a.blk_off[a.R] = carry[2];
   }
 }
 
@@ -110,6 +102,8 @@ constexpr int kRowTile2 = 32;   // query rows per shared-memory tile in pass 2
 
 // Pass 1: per item and query row, (m2, Z) of the causal softmax over the item's keys.
 __global__ void __launch_bounds__(kThreads) score_pass1_simt(const __grid_constant__ ScoreArgs a) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float smem[];
   const int item = blockIdx.x;
   if (item >= a.item_off1[a.R] || item >= a.items1) return;
@@ -174,6 +168,8 @@ __global__ void __launch_bounds__(kThreads) score_pass1_simt(const __grid_consta
 
 // Pass 2: per key, sum over the rows of one query chunk of 2^(x - lse2).
 __global__ void __launch_bounds__(kThreads) score_pass2_simt(const __grid_constant__ ScoreArgs a) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float smem[];
   const int item = blockIdx.x;
   if (item >= a.item_off2[a.R] || item >= a.items2) return;
@@ -250,29 +246,26 @@ size_t pass2_smem(int d, int QC) { return sizeof(float) * (QC + kThreads * (d + 
 
 }  // namespace
 
-cudaError_t launch_describe(const DescribeArgs& a, cudaStream_t s) {
-  describe_kernel<<<1, 1024, 0, s>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_describe(const DescribeArgs& a, cudaStream_t s, bool pdl) {
+  return launch_kernel(describe_kernel, 1, 32, 0, s, pdl, a);
 }
 
-cudaError_t launch_score_pass1(const ScoreArgs& a, cudaStream_t s) {
-  if (a.use_tc) return launch_score_pass1_tc(a, s);
+cudaError_t launch_score_pass1(const ScoreArgs& a, cudaStream_t s, bool pdl) {
+  if (a.use_tc) return launch_score_pass1_tc(a, s, pdl);
   if (a.items1 == 0) return cudaSuccess;
   const size_t smem = pass1_smem(a.d);
   cudaError_t e = cudaFuncSetAttribute(score_pass1_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  score_pass1_simt<<<a.items1, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(score_pass1_simt, a.items1, kThreads, smem, s, pdl, a);
 }
 
-cudaError_t launch_score_pass2(const ScoreArgs& a, cudaStream_t s) {
-  if (a.use_tc) return launch_score_pass2_tc(a, s);
+cudaError_t launch_score_pass2(const ScoreArgs& a, cudaStream_t s, bool pdl) {
+  if (a.use_tc) return launch_score_pass2_tc(a, s, pdl);
   if (a.items2 == 0) return cudaSuccess;
   const size_t smem = pass2_smem(a.d, a.QC);
   cudaError_t e = cudaFuncSetAttribute(score_pass2_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  score_pass2_simt<<<a.items2, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(score_pass2_simt, a.items2, kThreads, smem, s, pdl, a);
 }
 
 }  // namespace upf

@@ -189,11 +189,14 @@ upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p
       }
     const char* path = std::getenv("UPF_SCORE_PATH");
     pl->use_tc = pl->q_box_rows > 0 && !(path && std::strcmp(path, "simt") == 0);
-    // The split depends only on the batch and parameters (never on the device),
-    // so upf_workspace_bytes() without a context sizes exactly what a call uses.
+    // Key splits: the tensor-core kernels hold one CTA per SM, so one wave of
+    // about one item per SM; the CUDA-core kernels want a few waves.  The split
+    // depends only on the batch and parameters (never on the device), so
+    // upf_workspace_bytes() without a context sizes exactly what a call uses.
     (void)ctx;
-    pl->KS1 = choose_split(b, pl->Hkv * pl->NQC, 2LL * upf::kPlanSMs);
-    pl->KS2 = choose_split(b, pl->Hkv * pl->NQC, 4LL * upf::kPlanSMs);
+    const long long target = (pl->use_tc ? 1LL : 4LL) * upf::kPlanSMs;
+    pl->KS1 = choose_split(b, pl->Hkv * pl->NQC, target);
+    pl->KS2 = choose_split(b, pl->Hkv * pl->NQC, target);
     pl->items1 = pl->items2 = 0;
     pl->NB = 0;
     pl->max_nb = 0;
@@ -413,10 +416,11 @@ cudaError_t staged(upf_ctx* ctx, int stage, cudaStream_t s, F&& f) {
 
 enum Stage { kDescribe = 0, kPass1, kPass2, kFinalize, kSelect, kCompactCount, kCompactIndex, kCompactGather };
 
-upf_status launch_compact_all(upf_ctx* ctx, const upf::CompactArgs& ca, cudaStream_t s) {
-  UPF_LAUNCH(staged(ctx, kCompactCount, s, [&] { return upf::launch_compact_count(ca, s); }), "compact count");
-  UPF_LAUNCH(staged(ctx, kCompactIndex, s, [&] { return upf::launch_compact_index(ca, s); }), "compact index");
-  UPF_LAUNCH(staged(ctx, kCompactGather, s, [&] { return upf::launch_compact_gather(ca, s); }), "compact gather");
+// chained: the count kernel follows another kernel of the same call (PDL).
+upf_status launch_compact_all(upf_ctx* ctx, const upf::CompactArgs& ca, cudaStream_t s, bool chained) {
+  UPF_LAUNCH(staged(ctx, kCompactCount, s, [&] { return upf::launch_compact_count(ca, s, chained); }), "compact count");
+  UPF_LAUNCH(staged(ctx, kCompactIndex, s, [&] { return upf::launch_compact_index(ca, s, true); }), "compact index");
+  UPF_LAUNCH(staged(ctx, kCompactGather, s, [&] { return upf::launch_compact_gather(ca, s, true); }), "compact gather");
   return UPF_OK;
 }
 
@@ -576,13 +580,13 @@ upf_status upf_score(upf_ctx* ctx, const upf_batch* batch, const upf_params* par
   DeviceGuard guard(ctx->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const upf::DescribeArgs da = describe_args(ctx, batch, pl, ws);
-  UPF_LAUNCH(staged(ctx, kDescribe, s, [&] { return upf::launch_describe(da, s); }), "describe");
+  UPF_LAUNCH(staged(ctx, kDescribe, s, [&] { return upf::launch_describe(da, s, false); }), "describe");
   upf::ScoreArgs sa = score_args(ctx, batch, pl, q, q_row_stride, k, k_row_stride, ws);
-  UPF_LAUNCH(staged(ctx, kPass1, s, [&] { return upf::launch_score_pass1(sa, s); }), "score pass 1");
-  UPF_LAUNCH(staged(ctx, kPass2, s, [&] { return upf::launch_score_pass2(sa, s); }), "score pass 2");
+  UPF_LAUNCH(staged(ctx, kPass1, s, [&] { return upf::launch_score_pass1(sa, s, true); }), "score pass 1");
+  UPF_LAUNCH(staged(ctx, kPass2, s, [&] { return upf::launch_score_pass2(sa, s, true); }), "score pass 2");
   upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC, sa.part, nullptr, scores, nullptr,
                                    nullptr, nullptr);
-  UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s); }), "finalize scores");
+  UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s, true); }), "finalize scores");
   return UPF_OK;
 }
 
@@ -598,11 +602,11 @@ upf_status upf_select(upf_ctx* ctx, const upf_batch* batch, const upf_params* pa
   DeviceGuard guard(ctx->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const upf::DescribeArgs da = describe_args(ctx, batch, pl, ws);
-  UPF_LAUNCH(staged(ctx, kDescribe, s, [&] { return upf::launch_describe(da, s); }), "describe");
+  UPF_LAUNCH(staged(ctx, kDescribe, s, [&] { return upf::launch_describe(da, s, false); }), "describe");
   upf::SelectArgs se = select_args(ctx, batch, pl, ws, 0, nullptr, scores, nullptr, block_scores, keep_bits,
                                    kept_count);
-  UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s); }), "block means");
-  UPF_LAUNCH(staged(ctx, kSelect, s, [&] { return upf::launch_select(se, s); }), "select");
+  UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s, true); }), "block means");
+  UPF_LAUNCH(staged(ctx, kSelect, s, [&] { return upf::launch_select(se, s, true); }), "select");
   return UPF_OK;
 }
 
@@ -616,7 +620,48 @@ upf_status upf_compact(upf_ctx* ctx, const upf_batch* batch, const uint32_t* kee
   if ((st = check_compact_io(pl, keep_bits, io)) != UPF_OK) return st;
   DeviceGuard guard(ctx->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return launch_compact_all(ctx, compact_args(ctx, batch, pl, keep_bits, io, ws), s);
+  return launch_compact_all(ctx, compact_args(ctx, batch, pl, keep_bits, io, ws), s, false);
+  return UPF_OK;
+}
+
+upf_status upf_revive(upf_ctx* ctx, const upf_batch* batch, const int32_t* kept_index, const int32_t* total_kept,
+                      const void* rows, int64_t row_bytes, void* full, void* stream) {
+  upf_status st;
+  if ((st = check_ctx(ctx)) != UPF_OK) return st;
+  if ((st = check_batch(batch)) != UPF_OK) return st;
+  if (!kept_index || !total_kept || !rows || !full) return fail(UPF_ERR_INVALID_ARG, "kept_index, total_kept, rows and full are required");
+  if (row_bytes <= 0 || row_bytes % 16) return fail(UPF_ERR_INVALID_ARG, "row_bytes must be a positive multiple of 16");
+  if (!aligned16(rows) || !aligned16(full)) return fail(UPF_ERR_INVALID_ARG, "rows and full must be 16-byte aligned");
+  DeviceGuard guard(ctx->device);
+  upf::ReviveArgs a;
+  a.T = batch->cu_seqlens_host[batch->num_reqs];
+  a.kept_index = kept_index;
+  a.total_kept = total_kept;
+  a.rows = rows;
+  a.full = full;
+  a.row_bytes = row_bytes;
+  UPF_LAUNCH(upf::launch_revive(a, static_cast<cudaStream_t>(stream)), "revive");
+  return UPF_OK;
+}
+
+upf_status upf_history_kv_len(upf_ctx* ctx, const upf_batch* batch, const int32_t* history,
+                              const int32_t* history_len, int32_t history_cap, int32_t layer_id, int32_t* kv_len,
+                              void* stream) {
+  upf_status st;
+  if ((st = check_ctx(ctx)) != UPF_OK) return st;
+  if ((st = check_batch(batch)) != UPF_OK) return st;
+  if (!history || !history_len || !kv_len) return fail(UPF_ERR_INVALID_ARG, "history, history_len and kv_len are required");
+  if (history_cap < 1) return fail(UPF_ERR_INVALID_ARG, "history_cap must be >= 1");
+  DeviceGuard guard(ctx->device);
+  upf::HistoryArgs a;
+  a.cu = batch->cu_seqlens_dev;
+  a.R = batch->num_reqs;
+  a.layer_id = layer_id;
+  a.history_cap = history_cap;
+  a.history = history;
+  a.history_len = history_len;
+  a.kv_len = kv_len;
+  UPF_LAUNCH(upf::launch_history_kv_len(a, static_cast<cudaStream_t>(stream)), "history kv length");
   return UPF_OK;
 }
 
@@ -635,15 +680,15 @@ upf_status upf_select_tokens(upf_ctx* ctx, const upf_batch* batch, const upf_par
   DeviceGuard guard(ctx->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const upf::DescribeArgs da = describe_args(ctx, batch, pl, ws);
-  UPF_LAUNCH(staged(ctx, kDescribe, s, [&] { return upf::launch_describe(da, s); }), "describe");
+  UPF_LAUNCH(staged(ctx, kDescribe, s, [&] { return upf::launch_describe(da, s, false); }), "describe");
   upf::ScoreArgs sa = score_args(ctx, batch, pl, q, q_row_stride, k, k_row_stride, ws);
-  UPF_LAUNCH(staged(ctx, kPass1, s, [&] { return upf::launch_score_pass1(sa, s); }), "score pass 1");
-  UPF_LAUNCH(staged(ctx, kPass2, s, [&] { return upf::launch_score_pass2(sa, s); }), "score pass 2");
+  UPF_LAUNCH(staged(ctx, kPass1, s, [&] { return upf::launch_score_pass1(sa, s, true); }), "score pass 1");
+  UPF_LAUNCH(staged(ctx, kPass2, s, [&] { return upf::launch_score_pass2(sa, s, true); }), "score pass 2");
   upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC, sa.part, nullptr, scores, block_scores,
                                    keep_bits, kept_count);
-  UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s); }), "finalize scores");
-  UPF_LAUNCH(staged(ctx, kSelect, s, [&] { return upf::launch_select(se, s); }), "select");
-  return launch_compact_all(ctx, compact_args(ctx, batch, pl, keep_bits, io, ws), s);
+  UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s, true); }), "finalize scores");
+  UPF_LAUNCH(staged(ctx, kSelect, s, [&] { return upf::launch_select(se, s, true); }), "select");
+  return launch_compact_all(ctx, compact_args(ctx, batch, pl, keep_bits, io, ws), s, true);
   return UPF_OK;
 }
 

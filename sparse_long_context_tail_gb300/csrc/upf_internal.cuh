@@ -98,6 +98,47 @@ struct CompactArgs {
   int32_t* status;
 };
 
+struct ReviveArgs {
+  int32_t T;
+  const int32_t* kept_index;
+  const int32_t* total_kept;
+  const void* rows;
+  void* full;
+  int64_t row_bytes;
+};
+
+struct HistoryArgs {
+  const int32_t* cu;
+  int32_t R, layer_id, history_cap;
+  const int32_t* history;
+  const int32_t* history_len;
+  int32_t* kv_len;
+};
+
+// Programmatic dependent launch.  Kernels launched after the first one of an
+// API call may start while their predecessor is finishing; each kernel lets its
+// own dependent start early and waits for its predecessor (full completion and
+// memory visibility) before touching global memory.  Both are no-ops for a
+// kernel launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                 bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Device status word helpers: the first error code wins.
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);
@@ -107,16 +148,18 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
 void set_last_error(const char* msg);
 
 // Launchers (defined in the kernel translation units); all return cudaGetLastError().
-cudaError_t launch_describe(const DescribeArgs& a, cudaStream_t s);
-cudaError_t launch_score_pass1(const ScoreArgs& a, cudaStream_t s);
-cudaError_t launch_score_pass2(const ScoreArgs& a, cudaStream_t s);
-cudaError_t launch_score_pass1_tc(const ScoreArgs& a, cudaStream_t s);
-cudaError_t launch_score_pass2_tc(const ScoreArgs& a, cudaStream_t s);
+cudaError_t launch_describe(const DescribeArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_score_pass1(const ScoreArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_score_pass2(const ScoreArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_score_pass1_tc(const ScoreArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_score_pass2_tc(const ScoreArgs& a, cudaStream_t s, bool pdl = false);
 size_t score_tc_smem_bytes(int d, int QC);
-cudaError_t launch_block_means(const SelectArgs& a, cudaStream_t s);
-cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
-cudaError_t launch_compact_count(const CompactArgs& a, cudaStream_t s);
-cudaError_t launch_compact_index(const CompactArgs& a, cudaStream_t s);
-cudaError_t launch_compact_gather(const CompactArgs& a, cudaStream_t s);
+cudaError_t launch_block_means(const SelectArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_compact_count(const CompactArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_compact_index(const CompactArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_compact_gather(const CompactArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_revive(const ReviveArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_history_kv_len(const HistoryArgs& a, cudaStream_t s, bool pdl = false);
 
 }  // namespace upf

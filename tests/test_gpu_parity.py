@@ -349,3 +349,55 @@ def test_full_size_workload(sel, name):
     p = params_of(spec)
     out, status, inputs = run_gpu(sel, w, p)
     check(w, p, out, status, inputs)
+
+
+def _select_only(sel, scores_np, cu, block, top_p, sink=128, tail=128):
+    cu = np.asarray(cu, dtype=np.int32)
+    T, R = int(cu[-1]), len(cu) - 1
+    cu_dev = _up(cu)
+    batch, keep = B.make_batch(cu_dev.data_ptr(), cu, 1, 1, 64)
+    p = B.make_params(block=block, top_p=top_p, sink_keep=sink, tail_keep=tail)
+    nbytes = B.upf_workspace_bytes(batch, p)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    scores = _up(np.asarray(scores_np, dtype=np.float32))
+    nb = TokenSelectorBlocks(cu, block)
+    bs = torch.empty(max(1, nb), dtype=torch.float32, device=DEV)
+    bits = torch.empty((T + 31) // 32, dtype=torch.int32, device=DEV)
+    cnt = torch.empty(R, dtype=torch.int32, device=DEV)
+    B.upf_select(sel.ctx, batch, p, scores.data_ptr(), bs.data_ptr(), bits.data_ptr(), cnt.data_ptr(),
+                 ws.data_ptr(), nbytes, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    return sel.status(), C.unpack_bits(bits.cpu().numpy(), T), bs.cpu().numpy()[:nb], cnt.cpu().numpy()
+
+
+def test_select_ties_take_lower_blocks_first(sel):
+    """Equal block scores at the boundary enter in block-index order (the oracle's tie rule)."""
+    rng = np.random.default_rng(3)
+    for G, L, top_p in [(64, 64 * 300, 0.5), (32, 32 * 1000 + 17, 0.37), (16, 16 * 5000, 0.9)]:
+        nb = -(-L // G)
+        levels = np.array([0.0, 1.0, 2.0, 4.0], dtype=np.float32)    # few distinct values: many ties
+        b = levels[rng.integers(0, 4, size=nb)]
+        scores = np.repeat(b, G)[:L]
+        status, mask, bs, cnt = _select_only(sel, scores, [0, L], G, top_p, sink=0, tail=0)
+        assert status == 0
+        want = oracle.select(scores.astype(np.float64), [0, L], G, top_p, 0, 0)["mask"]
+        np.testing.assert_array_equal(mask, want)
+
+
+def test_select_rejects_negative_scores(sel):
+    scores = np.full(2000, 1.0 / 2000, dtype=np.float32)
+    scores[768:832] = -1e-3          # block 12 has a negative mean
+    status, mask, bs, cnt = _select_only(sel, scores, [0, 2000], 64, 0.99)
+    assert status == 5 and mask.all() and cnt.tolist() == [2000]
+
+
+def test_select_large_request_many_blocks(sel):
+    """16384 blocks (the per-request maximum) against the oracle's rule."""
+    rng = np.random.default_rng(4)
+    G, nb = 8, 16384
+    b = rng.exponential(1.0, size=nb).astype(np.float32) ** 4
+    scores = np.repeat(b, G)
+    status, mask, bs, cnt = _select_only(sel, scores, [0, nb * G], G, 0.95)
+    assert status == 0
+    bad = C.self_consistency_mismatches(mask, bs, [0, nb * G], G, 0.95, 128, 128)
+    assert not bad, bad[:5]

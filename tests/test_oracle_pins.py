@@ -402,3 +402,34 @@ def test_empty_request_in_a_batch():
     out = oracle.select_tokens(k, q, cu, 2, 1, 4, 8, 4, 0.9, 4, 4, threads=1)
     assert out["kept_count"].tolist()[1] == 0
     assert abs(out["scores"][:20].sum() - 1) < 1e-12 and abs(out["scores"][20:].sum() - 1) < 1e-12
+
+
+def test_history_kv_len_hand_worked():
+    """Two requests of 1000 and 600 tokens; drops at layers 3 and 11 for request 0, layer 3 only for request 1.
+
+    Layers 0-2 hold the prompt; layers 3-10 hold the first drop's kept count;
+    layer 11 on holds the second drop's (UniPrefill article, section 3: the
+    drop history tells decode how many KV entries each layer wrote).
+    """
+    hist = np.array([[[3, 400], [11, 150], [0, 0]], [[3, 90], [0, 0], [0, 0]]])
+    hlen = np.array([2, 1])
+    cu = [0, 1000, 1600]
+    want = {0: [1000, 600], 2: [1000, 600], 3: [400, 90], 10: [400, 90], 11: [150, 90], 40: [150, 90]}
+    for layer, kv in want.items():
+        assert oracle.history_kv_len(hist, hlen, cu, layer).tolist() == kv
+    assert oracle.history_kv_len(hist, np.array([0, 0]), cu, 40).tolist() == [1000, 600]
+
+
+def test_revive_hand_worked_and_round_trip():
+    """Kept rows return to their token positions; dropped rows stay frozen (section 2, third step)."""
+    full = np.arange(6 * 2).reshape(6, 2)            # 6 tokens, 2 values each
+    rows = np.array([[100, 101], [102, 103]])        # later layers' output for the kept tokens 1 and 4
+    got = oracle.revive(full, [1, 4], rows)
+    assert got.tolist() == [[0, 1], [100, 101], [4, 5], [6, 7], [102, 103], [10, 11]]
+    assert full.tolist()[1] == [2, 3]                 # input untouched
+    # compacting then reviving unchanged rows reproduces the original exactly
+    rng = np.random.default_rng(0)
+    h = rng.integers(0, 1 << 15, size=(50, 8))
+    mask = rng.random(50) < 0.3
+    comp = oracle.compact(mask, [0, 20, 50], hidden=h)
+    np.testing.assert_array_equal(oracle.revive(h, comp["kept_index"], comp["hidden_out"]), h)
