@@ -19,7 +19,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
-#include "../../include/upf.h"
+#include "upf.h"
 
 namespace upf {
 
