@@ -80,6 +80,7 @@ struct Plan {
   int n = 0, G = 0, sink = 0, tail = 0;
   float top_p = 0.f, scale = 0.f;
   int QR = 0, QC = 0, NQC = 0, KS1 = 0, KS2 = 0;
+  int pw = 1;   // partial rows per pass-1 item row and per (kv head, query chunk)
   int q_box_rows = 0;
   bool use_tc = false;
   long long items1 = 0, items2 = 0;
@@ -140,13 +141,14 @@ upf_status check_params(const upf_params* p) {
 
 int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
 
-// Keys per split so that the pass has about `target` items in total.
-int choose_split(const upf_batch* b, int per_req_units, long long target) {
+// Keys per split so that the pass has about `target` items in total: a
+// multiple of `tile` keys, at least 256.
+int choose_split(const upf_batch* b, int per_req_units, long long target, int tile) {
   long long keys = 0;
   for (int r = 0; r < b->num_reqs; ++r) keys += b->cu_seqlens_host[r + 1] - b->cu_seqlens_host[r];
   long long units = keys * per_req_units;
   long long ks = (units + target - 1) / std::max(1LL, target);
-  ks = ((ks + 127) / 128) * 128;
+  ks = ((ks + tile - 1) / tile) * tile;
   if (ks < 256) ks = 256;
   return int(std::min<long long>(ks, 1 << 30));
 }
@@ -195,8 +197,11 @@ upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p
     // upf_workspace_bytes() without a context sizes exactly what a call uses.
     (void)ctx;
     const long long target = (pl->use_tc ? 1LL : 4LL) * upf::kPlanSMs;
-    pl->KS1 = choose_split(b, pl->Hkv * pl->NQC, target);
-    pl->KS2 = choose_split(b, pl->Hkv * pl->NQC, target);
+    const int tile1 = pl->use_tc ? upf::score_tc_key_tile(1, pl->d) : 128;
+    const int tile2 = pl->use_tc ? upf::score_tc_key_tile(2, pl->d) : 128;
+    pl->KS1 = choose_split(b, pl->Hkv * pl->NQC, target, tile1);
+    pl->KS2 = choose_split(b, pl->Hkv * pl->NQC, target, tile2);
+    pl->pw = pl->use_tc ? upf::kTcPartials : 1;
     pl->items1 = pl->items2 = 0;
     pl->NB = 0;
     pl->max_nb = 0;
@@ -225,9 +230,9 @@ upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p
   pl->off_desc = off;
   off = align256(off + sizeof(int32_t) * 3 * (pl->R + 1));
   pl->off_p1 = off;
-  off = align256(off + sizeof(float2) * size_t(pl->items1) * pl->QC);
+  off = align256(off + sizeof(float2) * size_t(pl->items1) * pl->pw * pl->QC);
   pl->off_part = off;
-  off = align256(off + sizeof(float) * size_t(pl->Hkv) * pl->NQC * pl->T);
+  off = align256(off + sizeof(float) * size_t(pl->Hkv) * pl->NQC * pl->pw * pl->T);
   pl->off_bs = off;
   off = align256(off + sizeof(float) * size_t(pl->NB));
   pl->off_chunk = off;
@@ -312,6 +317,7 @@ upf::ScoreArgs score_args(const upf_ctx* ctx, const upf_batch* b, const Plan& pl
   a.use_tc = pl.use_tc ? 1 : 0;
   a.item_off1 = at<int32_t>(ws, pl.off_desc);
   a.item_off2 = at<int32_t>(ws, pl.off_desc) + (pl.R + 1);
+  a.pw = pl.pw;
   a.p1part = at<float2>(ws, pl.off_p1);
   a.part = at<float>(ws, pl.off_part);
   a.status = ctx->status_dev;
@@ -584,7 +590,7 @@ upf_status upf_score(upf_ctx* ctx, const upf_batch* batch, const upf_params* par
   upf::ScoreArgs sa = score_args(ctx, batch, pl, q, q_row_stride, k, k_row_stride, ws);
   UPF_LAUNCH(staged(ctx, kPass1, s, [&] { return upf::launch_score_pass1(sa, s, true); }), "score pass 1");
   UPF_LAUNCH(staged(ctx, kPass2, s, [&] { return upf::launch_score_pass2(sa, s, true); }), "score pass 2");
-  upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC, sa.part, nullptr, scores, nullptr,
+  upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC * pl.pw, sa.part, nullptr, scores, nullptr,
                                    nullptr, nullptr);
   UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s, true); }), "finalize scores");
   return UPF_OK;
@@ -684,7 +690,7 @@ upf_status upf_select_tokens(upf_ctx* ctx, const upf_batch* batch, const upf_par
   upf::ScoreArgs sa = score_args(ctx, batch, pl, q, q_row_stride, k, k_row_stride, ws);
   UPF_LAUNCH(staged(ctx, kPass1, s, [&] { return upf::launch_score_pass1(sa, s, true); }), "score pass 1");
   UPF_LAUNCH(staged(ctx, kPass2, s, [&] { return upf::launch_score_pass2(sa, s, true); }), "score pass 2");
-  upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC, sa.part, nullptr, scores, block_scores,
+  upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC * pl.pw, sa.part, nullptr, scores, block_scores,
                                    keep_bits, kept_count);
   UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s, true); }), "finalize scores");
   UPF_LAUNCH(staged(ctx, kSelect, s, [&] { return upf::launch_select(se, s, true); }), "select");

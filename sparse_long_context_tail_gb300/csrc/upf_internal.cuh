@@ -27,6 +27,10 @@ constexpr int kMaxHeads = 256;         // H_q limit (the q-head list travels by 
 constexpr int kMaxBlocksPerReq = 16384;  // select kernel sorts up to this many blocks in shared memory
 constexpr int kCompactChunkWords = 1024;  // keep-bit words per compaction chunk (32768 tokens)
 constexpr int kPlanSMs = 152;             // SM count the work split is planned for (GB300)
+// Partial rows the tensor-core passes write per (kv head, query chunk) and
+// per pass-1 item row: two epilogue warps split every unit's columns and keep
+// separate sums.
+constexpr int kTcPartials = 2;
 
 struct ScoreArgs {
   const __nv_bfloat16* q;
@@ -43,8 +47,9 @@ struct ScoreArgs {
   int32_t use_tc;            // 1: tcgen05 kernels, 0: CUDA-core kernels
   const int32_t* item_off1;  // [R+1]
   const int32_t* item_off2;  // [R+1]
-  float2* p1part;            // [items1][QC]
-  float* part;               // [Hkv*NQC][T]
+  float2* p1part;            // [items1][pw][QC]
+  float* part;               // [Hkv*NQC*pw][T]
+  int32_t pw;                // partial rows per item row / per (g, qc): kTcPartials or 1
   int32_t* status;
   int32_t qhead[kMaxHeads];  // q heads of group g at [g*gamma, (g+1)*gamma)
 };
@@ -153,7 +158,10 @@ cudaError_t launch_score_pass1(const ScoreArgs& a, cudaStream_t s, bool pdl = fa
 cudaError_t launch_score_pass2(const ScoreArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_score_pass1_tc(const ScoreArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_score_pass2_tc(const ScoreArgs& a, cudaStream_t s, bool pdl = false);
-size_t score_tc_smem_bytes(int d, int QC);
+// Dynamic shared memory of a tensor-core pass (1 or 2) for head dim d and QC
+// rows per query chunk, and its keys per tile (key splits are multiples of it).
+size_t score_tc_smem_bytes(int pass, int d, int QC);
+int score_tc_key_tile(int pass, int d);
 cudaError_t launch_block_means(const SelectArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_compact_count(const CompactArgs& a, cudaStream_t s, bool pdl = false);
