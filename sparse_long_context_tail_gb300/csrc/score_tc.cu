@@ -13,12 +13,15 @@
 //     lane is one key, so sum_q 2^(x*log2e*scale - lse2[q]) is a per-thread
 //     reduction along the columns.
 //
-// One CTA per work item (request, kv head, key split, query chunk), 10 warps:
-//   warps 0-7  epilogue: warp w reads TMEM lanes 32*(w%4).. and the column
-//              half w/4 of every unit, so all eight work on the same unit
-//   warp 8     TMA producer (lane 0): the query chunk once, then the key
+// One CTA per work item (request, kv head, key split, query chunk), 18 warps:
+//   warps 0-15 epilogue: warp w reads TMEM lanes 32*(w%4).. and the column
+//              quarter w/4 of every unit, so all sixteen work on the same
+//              unit (four warps per scheduler hide the exponential unit's and
+//              the TMEM loads' latency; two were measured to leave both the
+//              issue slots and the exponential unit 60% idle)
+//   warp 16    TMA producer (lane 0): the query chunk once, then the key
 //              tiles through a ring of 32 KB stages
-//   warp 9     TMEM allocator + MMA issuer (lane 0)
+//   warp 17    TMEM allocator + MMA issuer (lane 0)
 // A "unit" is one MMA accumulator of 128 lanes x up to 256 fp32 columns
 // (N = 256 keys per unit in pass 1, 256 query columns in pass 2; the M=128,
 // N=256 shape reads 12 KB of shared memory per 128 MMA clocks, where N = 128
@@ -43,19 +46,19 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kW = 2;                          // epilogue warps per TMEM lane quarter
-constexpr int kEpiWarps = 4 * kW;              // 8
-constexpr int kEpiThreads = kEpiWarps * 32;    // 256
-constexpr int kProducerWarp = kEpiWarps;       // 8
-constexpr int kMmaWarp = kEpiWarps + 1;        // 9
-constexpr int kThreadsTC = kEpiThreads + 64;   // 320
+constexpr int kW = 4;                          // epilogue warps per TMEM lane quarter
+constexpr int kEpiWarps = 4 * kW;              // 16
+constexpr int kEpiThreads = kEpiWarps * 32;    // 512
+constexpr int kProducerWarp = kEpiWarps;       // 16
+constexpr int kMmaWarp = kEpiWarps + 1;        // 17
+constexpr int kThreadsTC = kEpiThreads + 64;   // 576
 constexpr int kStageBytes = 32768;             // largest ring stage
 constexpr int kMaxStages = 8;
 constexpr int kMaxSlots = 4;
+constexpr int kRedTiles = 8;                   // pass 2: tiles of per-key sums in flight
 constexpr int kSmemLimit = 232448;             // opt-in dynamic shared memory per CTA
 constexpr long long kWaitLimit = 4000000000LL; // clock cycles (about 2 s)
-
-static_assert(kW == kTcPartials, "one partial row per epilogue column half");
+constexpr uint32_t kIdleNs = 4000;              // longest suspension of a waiting role per poll
 
 __host__ __device__ constexpr int imin(int a, int b) { return a < b ? a : b; }
 __host__ __device__ constexpr int imax(int a, int b) { return a > b ? a : b; }
@@ -69,11 +72,12 @@ struct Geo {
   int sps;          // slices per ring stage
   int spt;          // ring stages per tile
   int stage_bytes;
+  int unit_cols;    // MMA N of a unit: keys (pass 1) or query columns (pass 2)
   int slot_cols;    // TMEM columns per accumulator slot
   int nslots;
   int NS;           // ring stages
   int q_bytes;      // resident query chunk: S x QC rows x 128 B
-  int extra_bytes;  // pass 2: -lse2 and query positions per chunk row
+  int extra_bytes;  // pass 2: -lse2 and query positions per chunk row, per-key partial sums
   int smem;         // dynamic shared memory of the CTA
 };
 
@@ -85,10 +89,14 @@ __host__ __device__ inline Geo geometry(int pass, int d, int QC) {
   g.sps = imax(1, imin(g.S, kStageBytes / g.slice_bytes));
   g.spt = g.S / g.sps;
   g.stage_bytes = g.sps * g.slice_bytes;
+  // Pass 2 units are 256 query columns when the chunk is a multiple of 256
+  // rows, else 128; rows past the chunk's end are zero with lse2 = +inf, so
+  // full-width units are exact.
+  g.unit_cols = pass == 1 ? g.tile_keys : (QC % 256 == 0 ? 256 : 128);
   g.slot_cols = pass == 1 ? g.tile_keys : 256;
   g.nslots = 512 / g.slot_cols;
   g.q_bytes = g.S * QC * 128;
-  g.extra_bytes = pass == 2 ? 8 * QC : 0;
+  g.extra_bytes = pass == 2 ? 8 * QC + kRedTiles * kW * 128 * 4 : 0;
   const int fixed = 1024 /* alignment slack */ + g.q_bytes + g.extra_bytes +
                     8 * (2 * kMaxStages + 2 * kMaxSlots + 2) + 16;
   g.NS = imin(kMaxStages, (kSmemLimit - fixed) / g.stage_bytes);
@@ -102,6 +110,7 @@ struct Smem {
   unsigned char* ring;    // NS stages
   float* nlse;            // pass 2: -lse2 per chunk row (+inf rows: -inf)
   int* tq;                // pass 2: query position per chunk row (-1: none)
+  float* red;             // pass 2: [kRedTiles][kW][128] per-key sums of the column quarters
   uint64_t* bars;         // full[8], empty[8], tfull[4], tempty[4], qfull, fin
   uint32_t* tmem_slot;
   int* abort_flag;
@@ -116,6 +125,7 @@ __device__ __forceinline__ Smem carve(unsigned char* raw, const Geo& g, int QC) 
   p += g.NS * g.stage_bytes;
   s.nlse = reinterpret_cast<float*>(p);
   s.tq = reinterpret_cast<int*>(p + 4 * QC);
+  s.red = reinterpret_cast<float*>(p + 8 * QC);
   p += g.extra_bytes;
   s.bars = reinterpret_cast<uint64_t*>(p);
   p += 8 * (2 * kMaxStages + 2 * kMaxSlots + 2);
@@ -199,10 +209,9 @@ __device__ __forceinline__ int64_t item_index(const int32_t* item_off, int r, in
 // Rows of the query chunk present in this item: [0, rows_c).
 __device__ __forceinline__ int chunk_rows(const ScoreArgs& a, int qc) { return min(a.QC, a.QR - qc * a.QC); }
 
-// Zero the rows [rows_c, roundup128(rows_c)) of the query chunk (generic
-// stores, ordered before any MMA reads by the caller's proxy fence + barrier).
-__device__ __forceinline__ void zero_padding(const ScoreArgs& a, const Smem& sm, int rows_c) {
-  const int pad = ((rows_c + 127) / 128) * 128;
+// Zero the rows [rows_c, pad) of the query chunk (generic stores, ordered
+// before any MMA reads by the caller's proxy fence + barrier).
+__device__ __forceinline__ void zero_padding(const ScoreArgs& a, const Smem& sm, int rows_c, int pad) {
   const int n16 = (pad - rows_c) * 8;
   for (int s = 0; s < a.d / 64; ++s) {
     uint4* base = reinterpret_cast<uint4*>(sm.q + size_t(s) * a.QC * 128 + size_t(rows_c) * 128);
@@ -259,15 +268,21 @@ __device__ __forceinline__ void online_update32(const float (&v)[32], float sl, 
   m = mn;
 }
 
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+  float4 r;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "r"(addr));
+  return r;
+}
+
 // Pass-2 step, unmasked: acc += 2^(v * sl - lse2) over 32 query columns of one
-// key; nlse points at -lse2 of those columns in shared memory (16-byte aligned).
-__device__ __forceinline__ void normalised_sum32(const float (&v)[32], const float* nlse, float sl, uint64_t& acc0,
+// key; nlse is the shared-memory address of -lse2 of those columns (16-byte
+// aligned).
+__device__ __forceinline__ void normalised_sum32(const float (&v)[32], uint32_t nlse, float sl, uint64_t& acc0,
                                                  uint64_t& acc1) {
-  const float4* l4 = reinterpret_cast<const float4*>(nlse);
   const uint64_t sl2 = pack2(sl, sl);
 #pragma unroll
   for (int j = 0; j < 32; j += 4) {
-    const float4 l = l4[j / 4];
+    const float4 l = lds_f4(nlse + 4 * j);
     float a, b, c, d;
     unpack2(fma2(pack2(v[j], v[j + 1]), sl2, pack2(l.x, l.y)), a, b);
     unpack2(fma2(pack2(v[j + 2], v[j + 3]), sl2, pack2(l.z, l.w)), c, d);
@@ -298,7 +313,7 @@ __device__ __forceinline__ void release_slot(const Smem& sm, int slot, int lane)
 // false (and the abort flag set) on a timeout or another role's abort.
 __device__ __forceinline__ bool wait_slot(const ScoreArgs& a, const Smem& sm, int slot, uint32_t parity) {
   if (aborted(sm)) return false;
-  if (!mbar_wait(bar_tfull(sm, slot), parity, kWaitLimit)) {
+  if (!mbar_wait_idle(bar_tfull(sm, slot), parity, kWaitLimit, kIdleNs)) {
     abort_with_timeout(a, sm);
     return false;
   }
@@ -306,34 +321,34 @@ __device__ __forceinline__ bool wait_slot(const ScoreArgs& a, const Smem& sm, in
   return true;
 }
 
-// Drain this warp's chunks of a unit: `count` chunks of 32 columns at column
-// offsets first, first + step, ... from taddr (this warp's lane quarter and
-// the slot base).  Chunk c+1 is loaded while chunk c is reduced; the slot is
-// released as soon as the last load has landed, before the last reduction.
-// process(v, chunk) receives the 32 values and the chunk's column offset.
-template <class F>
-__device__ __forceinline__ void drain_unit(uint32_t taddr, int first, int step, int count, const Smem& sm, int slot,
-                                           int lane, F&& process) {
-  if (count <= 0) {
-    release_slot(sm, slot, lane);
-    return;
+// wait_slot with the common case first: the unit is already there.
+__device__ __forceinline__ bool wait_slot_fast(const ScoreArgs& a, const Smem& sm, int slot, uint32_t parity) {
+  if (mbar_try_wait(bar_tfull(sm, slot), parity)) {
+    tc_fence_after();
+    return true;
   }
+  return wait_slot(a, sm, slot, parity);
+}
+
+// This warp's share of a unit: CPW chunks of 32 columns at taddr, taddr +
+// step, ... (TMEM lane quarter and slot already in taddr).  Both loads are
+// issued before the first reduction; the slot is released once the last
+// load has landed, before the last reduction.  process(v, c) gets chunk c.
+template <int CPW, class F>
+__device__ __forceinline__ void drain(uint32_t taddr, uint32_t step, const Smem& sm, int slot, int lane, F&& process) {
+  static_assert(CPW == 1 || CPW == 2, "one or two chunks per warp and unit");
   float va[32], vb[32];
-  tmem_ld32(taddr + uint32_t(first), va);
-  int c = 0, col = first;
-  while (true) {
+  tmem_ld32(taddr, va);
+  tmem_wait_ld();
+  if (CPW == 2) {
+    tmem_ld32(taddr + step, vb);
+    process(va, 0);
     tmem_wait_ld();
-    if (c + 1 < count) tmem_ld32(taddr + uint32_t(col + step), vb);
-    else release_slot(sm, slot, lane);
-    process(va, col);
-    if (++c >= count) break;
-    col += step;
-    tmem_wait_ld();
-    if (c + 1 < count) tmem_ld32(taddr + uint32_t(col + step), va);
-    else release_slot(sm, slot, lane);
-    process(vb, col);
-    if (++c >= count) break;
-    col += step;
+    release_slot(sm, slot, lane);
+    process(vb, 1);
+  } else {
+    release_slot(sm, slot, lane);
+    process(va, 0);
   }
 }
 
@@ -359,7 +374,7 @@ __device__ int produce(const ScoreArgs& a, const CUtensorMap* tq_map, const CUte
   for (; q < total; ++q) {
     const int st = q % geo.NS;
     if (aborted(sm)) break;
-    if (!mbar_wait(bar_empty(sm, st), ((q / geo.NS) & 1) ^ 1, kWaitLimit)) {
+    if (!mbar_wait_idle(bar_empty(sm, st), ((q / geo.NS) & 1) ^ 1, kWaitLimit, kIdleNs)) {
       abort_with_timeout(a, sm);
       break;
     }
@@ -385,32 +400,31 @@ __device__ void drain_loads(const Smem& sm, const Geo& geo, int issued) {
 // One thread issues every unit's MMAs in order.  Pass 1 (keys_as_m false):
 // unit u of a tile is query rows [128u, 128u+128) (A) against the tile's
 // tile_keys keys (B, N = tile_keys).  Pass 2: the tile's 128 keys (A) against
-// query columns [256u, 256u + N_u) (B).  Before returning it waits for all of
+// query columns [W u, W u + W) (B, N = W = unit_cols).  Before returning it waits for all of
 // them to finish.
-__device__ void issue_mma(const ScoreArgs& a, const Smem& sm, const Geo& geo, int ntiles, int units, int qcols,
-                          uint32_t tmem, bool keys_as_m) {
-  bool ok = mbar_wait(bar_qfull(sm), 0, kWaitLimit);
+__device__ void issue_mma(const ScoreArgs& a, const Smem& sm, const Geo& geo, int ntiles, int units, uint32_t tmem,
+                          bool keys_as_m) {
+  bool ok = mbar_wait_idle(bar_qfull(sm), 0, kWaitLimit, kIdleNs);
   int uidx = 0;
   for (int i = 0; ok && i < ntiles; ++i) {
     for (int p = 0; p < geo.spt && ok; ++p) {
       const int q = i * geo.spt + p;
-      ok = mbar_wait(bar_full(sm, q % geo.NS), (q / geo.NS) & 1, kWaitLimit);
+      ok = mbar_wait_idle(bar_full(sm, q % geo.NS), (q / geo.NS) & 1, kWaitLimit, kIdleNs);
     }
     if (!ok) break;
     tc_fence_after();
     for (int u = 0; u < units && ok; ++u, ++uidx) {
       const int slot = uidx % geo.nslots;
-      ok = mbar_wait(bar_tempty(sm, slot), ((uidx / geo.nslots) & 1) ^ 1, kWaitLimit);
+      ok = mbar_wait_idle(bar_tempty(sm, slot), ((uidx / geo.nslots) & 1) ^ 1, kWaitLimit, kIdleNs);
       if (!ok) break;
       tc_fence_after();
-      const int n = keys_as_m ? min(256, qcols - 256 * u) : geo.tile_keys;
-      const uint32_t idesc = idesc_bf16_f32(128, uint32_t(n));
+      const uint32_t idesc = idesc_bf16_f32(128, uint32_t(geo.unit_cols));
       const uint32_t dt = tmem + uint32_t(slot * geo.slot_cols);
       for (int s = 0; s < geo.S; ++s) {
         const int q = i * geo.spt + s / geo.sps;
         const uint32_t kb =
             smem_u32(sm.ring + size_t(q % geo.NS) * geo.stage_bytes + size_t(s % geo.sps) * geo.slice_bytes);
-        const uint32_t qb = smem_u32(sm.q + size_t(s) * a.QC * 128 + size_t(u) * (keys_as_m ? 256 : 128) * 128);
+        const uint32_t qb = smem_u32(sm.q + size_t(s) * a.QC * 128 + size_t(u) * (keys_as_m ? geo.unit_cols : 128) * 128);
         const uint32_t am = keys_as_m ? kb : qb, bn = keys_as_m ? qb : kb;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
@@ -424,14 +438,14 @@ __device__ void issue_mma(const ScoreArgs& a, const Smem& sm, const Geo& geo, in
   if (!ok) abort_with_timeout(a, sm);
   // Every MMA this thread issued must be done before TMEM can be freed.
   mma_commit(bar_fin(sm));
-  mbar_wait(bar_fin(sm), 0, kWaitLimit);
+  mbar_wait_idle(bar_fin(sm), 0, kWaitLimit, kIdleNs);
 }
 
 // Common prologue of both passes: barriers, padding, TMEM; returns the TMEM base.
-__device__ __forceinline__ uint32_t setup(const ScoreArgs& a, const Smem& sm, int rows_c) {
+__device__ __forceinline__ uint32_t setup(const ScoreArgs& a, const Smem& sm, int rows_c, int pad) {
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) init_barriers(sm);
-  zero_padding(a, sm, rows_c);
+  zero_padding(a, sm, rows_c, pad);
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(sm.tmem_slot), 512);
     tmem_relinquish();
@@ -445,7 +459,97 @@ __device__ __forceinline__ uint32_t setup(const ScoreArgs& a, const Smem& sm, in
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory"); }
 
+// Pass 2: the kW column-quarter sums of key row `krow` of tile i, in order.
+__device__ __forceinline__ float red_sum(const float* red, int i, int krow) {
+  const float* r = red + (i % kRedTiles) * kW * 128 + krow;
+  float t = r[0];
+#pragma unroll
+  for (int c = 1; c < kW; ++c) t += r[c * 128];
+  return t;
+}
+
+
+
 // ------------------------------------------------------------- pass 1 -----
+
+// Epilogue of pass 1.  This thread is row 128h + 32qd + lane of every unit h
+// and covers the column quarter cb of it (CPW chunks of 32 keys); it keeps
+// (m, Z) of up to four rows in scalars (the loop over h is not unrolled, to
+// keep the code small).  At the end the quarters of every row are merged
+// through shared memory and one (m, Z) per row is stored.
+template <int CPW>
+__device__ __forceinline__ void pass1_epilogue(const ScoreArgs& a, const Smem& sm, const Geo& geo, const ItemTC& it,
+                                               int item, int rows_c, int MT, int k0, int ntiles, uint32_t tmem,
+                                               int warp, int lane) {
+  const int qd = warp & 3, cb = warp >> 2;
+  const int span = CPW * 32;   // = tile_keys / kW
+  const float sl = a.scale_log2;
+  const int r0 = qd * 32 + lane;
+  auto trow_of = [&](int h) {
+    const int row = h * 128 + r0;
+    return (h < MT && row < rows_c) ? it.L - a.n + (it.qc * a.QC + row) % a.n : -1;
+  };
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+  float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+  const uint32_t tbase = tmem + (uint32_t(qd * 32) << 16) + uint32_t(cb * span);
+  bool ok = true;
+  int uidx = 0;
+  for (int i = 0; ok && i < ntiles; ++i) {
+    const int kt = k0 + i * geo.tile_keys;   // request-relative first key of the tile
+    const bool masked = kt + geo.tile_keys - 1 > it.L - a.n;
+#pragma unroll 1
+    for (int h = 0; h < MT; ++h, ++uidx) {
+      const int slot = uidx % geo.nslots;
+      if (!wait_slot_fast(a, sm, slot, (uidx / geo.nslots) & 1)) {
+        ok = false;
+        break;
+      }
+      const int trow = trow_of(h);
+      float mh = h == 0 ? m0 : h == 1 ? m1 : h == 2 ? m2 : m3;
+      float zh = h == 0 ? z0 : h == 1 ? z1 : h == 2 ? z2 : z3;
+      const int lim = trow - kt - cb * span;   // this warp's columns j > lim are invisible
+      const bool live = trow >= 0;
+      drain<CPW>(tbase + uint32_t(slot * geo.slot_cols), 32u, sm, slot, lane, [&](float (&v)[32], int c) {
+        if (masked) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (32 * c + j > lim) v[j] = -INFINITY;
+        }
+        if (live) online_update32(v, sl, mh, zh);
+      });
+      if (h == 0) { m0 = mh; z0 = zh; }
+      else if (h == 1) { m1 = mh; z1 = zh; }
+      else if (h == 2) { m2 = mh; z2 = zh; }
+      else { m3 = mh; z3 = zh; }
+    }
+  }
+  // The ring is idle here: every MMA, hence every load, finished before the
+  // last unit was read.
+  float2* red = reinterpret_cast<float2*>(sm.ring);   // [kW][QC]
+  if (ok) {
+    red[cb * a.QC + r0] = make_float2(m0, z0);
+    if (MT > 1) red[cb * a.QC + 128 + r0] = make_float2(m1, z1);
+    if (MT > 2) red[cb * a.QC + 256 + r0] = make_float2(m2, z2);
+    if (MT > 3) red[cb * a.QC + 384 + r0] = make_float2(m3, z3);
+  }
+  epi_bar();
+  if (!ok || aborted(sm)) return;
+  for (int row = cb * 128 + r0; row < MT * 128; row += kW * 128) {
+    if (row >= rows_c) continue;
+    float mm = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kW; ++c) mm = fmaxf(mm, red[c * a.QC + row].x);
+    float zz = 0.f;
+    if (mm > -INFINITY) {
+#pragma unroll
+      for (int c = 0; c < kW; ++c) {
+        const float2 p = red[c * a.QC + row];
+        if (p.y > 0.f) zz += p.y * ex2_approx(p.x - mm);
+      }
+    }
+    a.p1part[(int64_t)item * a.QC + row] = make_float2(mm, zz);
+  }
+}
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
     score_pass1_tc(const __grid_constant__ CUtensorMap tq_map, const __grid_constant__ CUtensorMap tk_map,
@@ -463,66 +567,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   const int ntiles = ceil_div_dev(k1 - k0, geo.tile_keys);
   const int MT = (rows_c + 127) / 128;   // units per tile: 128-row blocks of the chunk
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t tmem = setup(a, sm, rows_c);
+  const uint32_t tmem = setup(a, sm, rows_c, MT * 128);
 
   int issued = 0;
   if (warp == kProducerWarp) {
     if (lane == 0) issued = produce(a, &tq_map, &tk_map, sm, geo, it, rows_c, k0, ntiles);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) issue_mma(a, sm, geo, ntiles, MT, 0, tmem, false);
+    if (lane == 0) issue_mma(a, sm, geo, ntiles, MT, tmem, false);
+  } else if (geo.tile_keys / kW == 64) {
+    pass1_epilogue<2>(a, sm, geo, it, item, rows_c, MT, k0, ntiles, tmem, warp, lane);
   } else {
-    // Epilogue: this thread is row 128h + 32qd + lane of every unit h and
-    // covers the column half cb of it; it keeps (m, Z) of up to four rows.
-    const int qd = warp & 3, cb = warp >> 2;
-    const int half = geo.tile_keys / 2;
-    const float sl = a.scale_log2;
-    float m[4], z[4];
-    int trow[4];
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const int row = h * 128 + qd * 32 + lane;
-      m[h] = -INFINITY;
-      z[h] = 0.f;
-      trow[h] = (h < MT && row < rows_c) ? it.L - a.n + (it.qc * a.QC + row) % a.n : -1;
-    }
-    const uint32_t tbase = tmem + (uint32_t(qd * 32) << 16) + uint32_t(cb * half);
-    bool ok = true;
-    int uidx = 0;
-    for (int i = 0; ok && i < ntiles; ++i) {
-      const int kt = k0 + i * geo.tile_keys;                // request-relative first key of the tile
-      const bool masked = kt + geo.tile_keys - 1 > it.L - a.n;
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        if (h >= MT) break;
-        const int slot = uidx % geo.nslots;
-        const uint32_t parity = (uidx / geo.nslots) & 1;
-        ++uidx;
-        if (!wait_slot(a, sm, slot, parity)) {
-          ok = false;
-          break;
-        }
-        const int lim = trow[h] - kt - cb * half;   // this warp's columns j > lim are invisible
-        const bool live = trow[h] >= 0;
-        float& mh = m[h];
-        float& zh = z[h];
-        drain_unit(tbase + uint32_t(slot * geo.slot_cols), 0, 32, half / 32, sm, slot, lane,
-                   [&](float (&v)[32], int col) {
-                     if (masked) {
-#pragma unroll
-                       for (int j = 0; j < 32; ++j)
-                         if (col + j > lim) v[j] = -INFINITY;
-                     }
-                     if (live) online_update32(v, sl, mh, zh);
-                   });
-      }
-    }
-    if (ok) {
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int row = h * 128 + qd * 32 + lane;
-        if (h < MT && row < rows_c) a.p1part[((int64_t)item * kW + cb) * a.QC + row] = make_float2(m[h], z[h]);
-      }
-    }
+    pass1_epilogue<1>(a, sm, geo, it, item, rows_c, MT, k0, ntiles, tmem, warp, lane);
   }
   // Wind down: outstanding loads of an aborted pipeline, then free TMEM.
   if (warp == kProducerWarp && lane == 0 && aborted(sm)) drain_loads(sm, geo, issued);
@@ -532,6 +587,66 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 }
 
 // ------------------------------------------------------------- pass 2 -----
+
+// Epilogue of pass 2.  This thread is key 32qd + lane of every tile; its warp
+// reads the 32-column chunks cb and cb + kW (CPW of them) of every unit and
+// stores its per-key sum in red[i % kRedTiles][cb] without waiting.  A warp
+// holding unit x knows every warp released unit x - 2 (the MMA reuses a slot
+// only after that), so every warp finished all tiles before the one holding
+// unit x - 2, stores included (mbarrier arrive/wait order them): with two or
+// more units per tile, tile i - 2 is complete once a warp holds tile i, with
+// one unit tile i - 3 (the lag D).  The quarter's first warp adds the kW sums
+// of tile i - D in a fixed order (so results are reproducible) and writes
+// them out at the start of tile i; a row is rewritten D tiles after that read
+// is known done (kRedTiles >= 2D); the last D tiles go out after a barrier.
+template <int CPW>
+__device__ __forceinline__ void pass2_epilogue(const ScoreArgs& a, const Smem& sm, const Geo& geo, const ItemTC& it,
+                                               int U, int k0, int k1, int ntiles, uint32_t tmem, int warp,
+                                               int lane) {
+  const int qd = warp & 3, cb = warp >> 2;
+  const int krow = qd * 32 + lane;
+  const float sl = a.scale_log2;
+  float* out = a.part + (int64_t)(it.g * a.NQC + it.qc) * a.T + it.tok0;
+  const uint32_t tq = tmem + (uint32_t(qd * 32) << 16) + uint32_t(cb * 32);
+  const int lag = U >= 2 ? 2 : 3;
+  const uint32_t nlse_s = smem_u32(sm.nlse);
+  static_assert(kRedTiles >= 6, "rows are read lag tiles after their stores and rewritten lag tiles later");
+  bool ok = true;
+  int uidx = 0;
+  for (int i = 0; i < ntiles; ++i) {
+    const int kt = k0 + i * geo.tile_keys;
+    const int key = kt + krow;
+    const bool masked = kt + geo.tile_keys - 1 > it.L - a.n;
+    uint64_t acc0 = pack2(0.f, 0.f), acc1 = pack2(0.f, 0.f);
+    for (int u = 0; u < U; ++u, ++uidx) {
+      const int slot = uidx & 1;
+      if (!wait_slot_fast(a, sm, slot, (uidx >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      if (u == 0 && cb == 0 && i >= lag) {   // tile i - lag is complete: write it out
+        const int kprev = key - lag * geo.tile_keys;
+        if (kprev < k1) out[kprev] = red_sum(sm.red, i - lag, krow);
+      }
+      const int col0 = u * geo.unit_cols + cb * 32;
+      drain<CPW>(tq + uint32_t(slot * 256), uint32_t(32 * kW), sm, slot, lane, [&](float (&v)[32], int c) {
+        const int col = col0 + c * 32 * kW;
+        if (!masked) normalised_sum32(v, nlse_s + 4 * col, sl, acc0, acc1);
+        else acc0 = add2(acc0, pack2(normalised_sum32_masked(v, sm.nlse + col, sm.tq + col, key, sl), 0.f));
+      });
+    }
+    if (!ok) break;
+    float lo, hi;
+    unpack2(add2(acc0, acc1), lo, hi);
+    sm.red[((i % kRedTiles) * kW + cb) * 128 + krow] = lo + hi;
+  }
+  epi_bar();
+  if (ok && cb == 0 && !aborted(sm))
+    for (int i = max(0, ntiles - lag); i < ntiles; ++i) {
+      const int key = k0 + i * geo.tile_keys + krow;
+      if (key < k1) out[key] = red_sum(sm.red, i, krow);
+    }
+}
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
     score_pass2_tc(const __grid_constant__ CUtensorMap tq_map, const __grid_constant__ CUtensorMap tk_map,
@@ -545,23 +660,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   const Smem sm = carve(smem_raw, geo, a.QC);
   const ItemTC it = locate_tc(a.item_off2, a.cu, a.R, item, a.KS2, a.NQC);
   const int rows_c = chunk_rows(a, it.qc);
-  const int qcols = ((rows_c + 31) / 32) * 32;   // MMA columns (query rows, zero-padded)
-  const int U = (qcols + 255) / 256;             // units per tile
+  const int U = (rows_c + geo.unit_cols - 1) / geo.unit_cols;   // units per tile
+  const int qcols = U * geo.unit_cols;                         // MMA columns (zero-padded query rows)
   const int k0 = it.s * a.KS2, k1 = min(it.L, k0 + a.KS2);
   const int ntiles = ceil_div_dev(k1 - k0, geo.tile_keys);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t tmem = setup(a, sm, rows_c);
+  const uint32_t tmem = setup(a, sm, rows_c, qcols);
 
   int issued = 0;
   if (warp == kProducerWarp) {
     if (lane == 0) issued = produce(a, &tq_map, &tk_map, sm, geo, it, rows_c, k0, ntiles);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) issue_mma(a, sm, geo, ntiles, U, qcols, tmem, true);
+    if (lane == 0) issue_mma(a, sm, geo, ntiles, U, tmem, true);
   } else {
     // lse2 of every query row of the chunk from the pass-1 partials (all key
-    // splits, both column halves), stored negated; -inf marks rows that do
-    // not exist (padding, or positions before the request start).  The MMA
-    // runs meanwhile: the first unit is not read before this is done.
+    // splits), stored negated; -inf marks rows that do not exist (padding,
+    // or positions before the request start).  The MMA runs meanwhile: the
+    // first unit is not read before this is done.
     const int nsplit1 = ceil_div_dev(it.L, a.KS1);
     for (int row = tid; row < qcols; row += kEpiThreads) {
       float l2 = INFINITY;
@@ -569,18 +684,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       if (row < rows_c) {
         t = it.L - a.n + (it.qc * a.QC + row) % a.n;
         float mm = -INFINITY;
-        for (int s = 0; s < nsplit1; ++s) {
-          const int64_t base = item_index(a.item_off1, it.r, it.g, s, it.qc, nsplit1, a.NQC) * kW;
-          for (int c = 0; c < kW; ++c) mm = fmaxf(mm, a.p1part[(base + c) * a.QC + row].x);
-        }
+        for (int s = 0; s < nsplit1; ++s)
+          mm = fmaxf(mm, a.p1part[item_index(a.item_off1, it.r, it.g, s, it.qc, nsplit1, a.NQC) * a.QC + row].x);
         float Z = 0.f;
         if (mm > -INFINITY)
           for (int s = 0; s < nsplit1; ++s) {
-            const int64_t base = item_index(a.item_off1, it.r, it.g, s, it.qc, nsplit1, a.NQC) * kW;
-            for (int c = 0; c < kW; ++c) {
-              const float2 p = a.p1part[(base + c) * a.QC + row];
-              if (p.y > 0.f) Z += p.y * exp2f(p.x - mm);
-            }
+            const float2 p = a.p1part[item_index(a.item_off1, it.r, it.g, s, it.qc, nsplit1, a.NQC) * a.QC + row];
+            if (p.y > 0.f) Z += p.y * exp2f(p.x - mm);
           }
         if (Z > 0.f && t >= 0) l2 = mm + log2f(Z);
         else t = -1;
@@ -589,43 +699,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       sm.tq[row] = t;
     }
     epi_bar();
-    // Epilogue: this thread is key 32qd + lane of every tile; its warp reads
-    // the 32-column chunks cb, cb+2, ... of every unit.  The per-key sums of
-    // the two column halves go to separate partial rows, added up later.
-    const int qd = warp & 3, cb = warp >> 2;
-    const int krow = qd * 32 + lane;
-    const float sl = a.scale_log2;
-    float* out = a.part + (int64_t)((it.g * a.NQC + it.qc) * kW + cb) * a.T + it.tok0;
-    const uint32_t tbase = tmem + (uint32_t(qd * 32) << 16);
-    bool ok = true;
-    int uidx = 0;
-    for (int i = 0; ok && i < ntiles; ++i) {
-      const int kt = k0 + i * geo.tile_keys;
-      const int key = kt + krow;
-      const bool masked = kt + geo.tile_keys - 1 > it.L - a.n;
-      uint64_t acc0 = pack2(0.f, 0.f), acc1 = pack2(0.f, 0.f);
-      float accm = 0.f;
-      for (int u = 0; u < U; ++u, ++uidx) {
-        const int slot = uidx % geo.nslots;
-        if (!wait_slot(a, sm, slot, (uidx / geo.nslots) & 1)) {
-          ok = false;
-          break;
-        }
-        const int nch = min(256, qcols - 256 * u) / 32;
-        const int cnt = nch > cb ? (nch - cb + 1) / 2 : 0;
-        const float* nl = sm.nlse + 256 * u;
-        const int* tqu = sm.tq + 256 * u;
-        drain_unit(tbase + uint32_t(slot * geo.slot_cols), cb * 32, 64, cnt, sm, slot, lane,
-                   [&](float (&v)[32], int col) {
-                     if (!masked) normalised_sum32(v, nl + col, sl, acc0, acc1);
-                     else accm += normalised_sum32_masked(v, nl + col, tqu + col, key, sl);
-                   });
-      }
-      if (!ok) break;
-      float lo, hi;
-      unpack2(add2(acc0, acc1), lo, hi);
-      if (key < k1) out[key] = (lo + hi) + accm;
-    }
+    if (geo.unit_cols == 256) pass2_epilogue<2>(a, sm, geo, it, U, k0, k1, ntiles, tmem, warp, lane);
+    else pass2_epilogue<1>(a, sm, geo, it, U, k0, k1, ntiles, tmem, warp, lane);
   }
   if (warp == kProducerWarp && lane == 0 && aborted(sm)) drain_loads(sm, geo, issued);
   tc_fence_before();

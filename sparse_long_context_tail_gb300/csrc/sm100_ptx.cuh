@@ -72,6 +72,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long lo
   return true;
 }
 
+// As mbar_try_wait, but an incomplete phase may suspend the thread for up to
+// `ns` nanoseconds (it resumes as soon as the phase completes).  For roles
+// with nothing else to do while they wait: a suspended thread issues nothing,
+// so its polling does not take issue slots from the warps that share its
+// scheduler.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait for an idle role: suspends between polls; false on timeout.
+__device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity, long long limit, uint32_t ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_hint(bar, parity, ns)) {
+    if (clock64() - t0 > limit) return false;
+  }
+  return true;
+}
+
 // ----------------------------------------------------------------- TMA ----
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int c0, int c1, uint32_t bar) {

@@ -28,9 +28,9 @@ constexpr int kMaxBlocksPerReq = 16384;  // select kernel sorts up to this many 
 constexpr int kCompactChunkWords = 1024;  // keep-bit words per compaction chunk (32768 tokens)
 constexpr int kPlanSMs = 152;             // SM count the work split is planned for (GB300)
 // Partial rows the tensor-core passes write per (kv head, query chunk) and
-// per pass-1 item row: two epilogue warps split every unit's columns and keep
-// separate sums.
-constexpr int kTcPartials = 2;
+// per pass-1 item row (the epilogue warps that split a unit's columns merge
+// their sums inside the CTA).
+constexpr int kTcPartials = 1;
 
 struct ScoreArgs {
   const __nv_bfloat16* q;
