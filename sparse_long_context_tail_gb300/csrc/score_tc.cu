@@ -35,6 +35,7 @@
 // is freed and the kernel returns.
 #include <cuda.h>
 
+#include <climits>
 #include <cmath>
 
 #include "sm100_ptx.cuh"
@@ -404,36 +405,50 @@ __device__ void drain_loads(const Smem& sm, const Geo& geo, int issued) {
 // them to finish.
 __device__ void issue_mma(const ScoreArgs& a, const Smem& sm, const Geo& geo, int ntiles, int units, uint32_t tmem,
                           bool keys_as_m) {
+  // Division-free bookkeeping: this thread shares its scheduler with busy
+  // epilogue warps, so every instruction between two MMAs costs issue slots.
+  const uint32_t idesc = idesc_bf16_f32(128, uint32_t(geo.unit_cols));
+  const uint32_t ring0 = smem_u32(sm.ring), q0 = smem_u32(sm.q);
+  const uint32_t q_slice = uint32_t(a.QC) * 128u;
+  const uint32_t q_unit = uint32_t(keys_as_m ? geo.unit_cols : 128) * 128u;
   bool ok = mbar_wait_idle(bar_qfull(sm), 0, kWaitLimit, kIdleNs);
-  int uidx = 0;
+  int st = 0;            // ring stage of the next tile's first part
+  uint32_t ph = 0;       // its phase parity
+  int slot = 0;          // TMEM slot of the next unit
+  uint32_t sph = 0;      // its phase parity
   for (int i = 0; ok && i < ntiles; ++i) {
-    for (int p = 0; p < geo.spt && ok; ++p) {
-      const int q = i * geo.spt + p;
-      ok = mbar_wait_idle(bar_full(sm, q % geo.NS), (q / geo.NS) & 1, kWaitLimit, kIdleNs);
-    }
+    // A tile takes spt <= 2 consecutive ring stages; slice s lives in stage
+    // part s / sps at offset (s % sps) slices, sps in {1, 2}.
+    const int st0 = st, st1 = st + 1 == geo.NS ? 0 : st + 1;
+    ok = mbar_wait_idle(bar_full(sm, st0), ph, kWaitLimit, kIdleNs);
+    if (ok && geo.spt == 2) ok = mbar_wait_idle(bar_full(sm, st1), st1 == 0 ? ph ^ 1u : ph, kWaitLimit, kIdleNs);
+    if (geo.spt == 2) { st = st1 + 1 == geo.NS ? 0 : st1 + 1; ph = (st1 == 0 || st == 0) ? ph ^ 1u : ph; }
+    else { st = st1; ph = st1 == 0 ? ph ^ 1u : ph; }
+    const uint32_t k0a = ring0 + uint32_t(st0 * geo.stage_bytes), k1a = ring0 + uint32_t(st1 * geo.stage_bytes);
     if (!ok) break;
     tc_fence_after();
-    for (int u = 0; u < units && ok; ++u, ++uidx) {
-      const int slot = uidx % geo.nslots;
-      ok = mbar_wait_idle(bar_tempty(sm, slot), ((uidx / geo.nslots) & 1) ^ 1, kWaitLimit, kIdleNs);
+    for (int u = 0; u < units; ++u) {
+      ok = mbar_wait_idle(bar_tempty(sm, slot), sph ^ 1u, kWaitLimit, kIdleNs);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t idesc = idesc_bf16_f32(128, uint32_t(geo.unit_cols));
       const uint32_t dt = tmem + uint32_t(slot * geo.slot_cols);
+      const uint32_t qu = q0 + uint32_t(u) * q_unit;
       for (int s = 0; s < geo.S; ++s) {
-        const int q = i * geo.spt + s / geo.sps;
-        const uint32_t kb =
-            smem_u32(sm.ring + size_t(q % geo.NS) * geo.stage_bytes + size_t(s % geo.sps) * geo.slice_bytes);
-        const uint32_t qb = smem_u32(sm.q + size_t(s) * a.QC * 128 + size_t(u) * (keys_as_m ? geo.unit_cols : 128) * 128);
-        const uint32_t am = keys_as_m ? kb : qb, bn = keys_as_m ? qb : kb;
+        const int part = geo.sps == 2 ? (s >> 1) : s;
+        const uint32_t kb = (part == 0 ? k0a : k1a) + uint32_t(geo.sps == 2 ? (s & 1) * geo.slice_bytes : 0);
+        const uint32_t qb = qu + uint32_t(s) * q_slice;
+        const uint64_t da = sdesc_kmajor_sw128(keys_as_m ? kb : qb);
+        const uint64_t db = sdesc_kmajor_sw128(keys_as_m ? qb : kb);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16(dt, sdesc_kmajor_sw128(am + kk * 32), sdesc_kmajor_sw128(bn + kk * 32), idesc, (s | kk) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk)   // +32 bytes along K = +2 in the descriptors' address field
+          mma_bf16(dt, da + uint64_t(2 * kk), db + uint64_t(2 * kk), idesc, (s | kk) ? 1u : 0u);
       }
       mma_commit(bar_tfull(sm, slot));
+      if (++slot == geo.nslots) { slot = 0; sph ^= 1u; }
     }
     if (!ok) break;
-    for (int p = 0; p < geo.spt; ++p) mma_commit(bar_empty(sm, (i * geo.spt + p) % geo.NS));
+    mma_commit(bar_empty(sm, st0));
+    if (geo.spt == 2) mma_commit(bar_empty(sm, st1));
   }
   if (!ok) abort_with_timeout(a, sm);
   // Every MMA this thread issued must be done before TMEM can be freed.
@@ -474,8 +489,7 @@ __device__ __forceinline__ float red_sum(const float* red, int i, int krow) {
 
 // Epilogue of pass 1.  This thread is row 128h + 32qd + lane of every unit h
 // and covers the column quarter cb of it (CPW chunks of 32 keys); it keeps
-// (m, Z) of up to four rows in scalars (the loop over h is not unrolled, to
-// keep the code small).  At the end the quarters of every row are merged
+// (m, Z) of up to four rows in registers.  At the end the quarters of every row are merged
 // through shared memory and one (m, Z) per row is stored.
 template <int CPW>
 __device__ __forceinline__ void pass1_epilogue(const ScoreArgs& a, const Smem& sm, const Geo& geo, const ItemTC& it,
@@ -485,10 +499,13 @@ __device__ __forceinline__ void pass1_epilogue(const ScoreArgs& a, const Smem& s
   const int span = CPW * 32;   // = tile_keys / kW
   const float sl = a.scale_log2;
   const int r0 = qd * 32 + lane;
-  auto trow_of = [&](int h) {
+  // Per row: the last key this warp's columns may see, relative to the
+  // tile's first key (INT_MIN: not a row of the chunk).
+  auto lim_of = [&](int h) {
     const int row = h * 128 + r0;
-    return (h < MT && row < rows_c) ? it.L - a.n + (it.qc * a.QC + row) % a.n : -1;
+    return (h < MT && row < rows_c) ? it.L - a.n + (it.qc * a.QC + row) % a.n - cb * span : INT_MIN;
   };
+  const int l0 = lim_of(0), l1 = lim_of(1), l2 = lim_of(2), l3 = lim_of(3);
   float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
   float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
   const uint32_t tbase = tmem + (uint32_t(qd * 32) << 16) + uint32_t(cb * span);
@@ -497,18 +514,19 @@ __device__ __forceinline__ void pass1_epilogue(const ScoreArgs& a, const Smem& s
   for (int i = 0; ok && i < ntiles; ++i) {
     const int kt = k0 + i * geo.tile_keys;   // request-relative first key of the tile
     const bool masked = kt + geo.tile_keys - 1 > it.L - a.n;
-#pragma unroll 1
-    for (int h = 0; h < MT; ++h, ++uidx) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h, ++uidx) {
+      if (h >= MT) break;
       const int slot = uidx % geo.nslots;
       if (!wait_slot_fast(a, sm, slot, (uidx / geo.nslots) & 1)) {
         ok = false;
         break;
       }
-      const int trow = trow_of(h);
+      const int lh = h == 0 ? l0 : h == 1 ? l1 : h == 2 ? l2 : l3;
       float mh = h == 0 ? m0 : h == 1 ? m1 : h == 2 ? m2 : m3;
       float zh = h == 0 ? z0 : h == 1 ? z1 : h == 2 ? z2 : z3;
-      const int lim = trow - kt - cb * span;   // this warp's columns j > lim are invisible
-      const bool live = trow >= 0;
+      const bool live = lh != INT_MIN;
+      const int lim = live ? lh - kt : 0;   // this warp's columns j > lim are invisible
       drain<CPW>(tbase + uint32_t(slot * geo.slot_cols), 32u, sm, slot, lane, [&](float (&v)[32], int c) {
         if (masked) {
 #pragma unroll
