@@ -371,19 +371,20 @@ __device__ int produce(const ScoreArgs& a, const CUtensorMap* tq_map, const CUte
                   bar_qfull(sm));
   }
   const int total = ntiles * geo.spt;
-  int q = 0;
+  int q = 0, st = 0, part = 0, key = it.tok0 + k0;
+  uint32_t ph = 0;
   for (; q < total; ++q) {
-    const int st = q % geo.NS;
     if (aborted(sm)) break;
-    if (!mbar_wait_idle(bar_empty(sm, st), ((q / geo.NS) & 1) ^ 1, kWaitLimit, kIdleNs)) {
+    if (!mbar_wait_idle(bar_empty(sm, st), ph ^ 1u, kWaitLimit, kIdleNs)) {
       abort_with_timeout(a, sm);
       break;
     }
-    const int i = q / geo.spt, part = q % geo.spt;
     mbar_arrive_expect_tx(bar_full(sm, st), uint32_t(geo.stage_bytes));
+    const uint32_t dst = smem_u32(sm.ring) + uint32_t(st * geo.stage_bytes);
     for (int ss = 0; ss < geo.sps; ++ss)
-      tma_load_3d(smem_u32(sm.ring + size_t(st) * geo.stage_bytes + size_t(ss) * geo.slice_bytes), tk_map,
-                  (part * geo.sps + ss) * 64, it.g, it.tok0 + k0 + i * geo.tile_keys, bar_full(sm, st));
+      tma_load_3d(dst + uint32_t(ss * geo.slice_bytes), tk_map, (part * geo.sps + ss) * 64, it.g, key, bar_full(sm, st));
+    if (++st == geo.NS) { st = 0; ph ^= 1u; }
+    if (++part == geo.spt) { part = 0; key += geo.tile_keys; }
   }
   return q;
 }
