@@ -248,31 +248,31 @@ __device__ __forceinline__ float max32(const float (&v)[32]) {
   return fmaxf(max3(max3(t[0], t[1], t[2]), max3(t[3], t[4], t[5]), max3(t[6], t[7], t[8])), fmaxf(t[9], t[10]));
 }
 
-// Pass-1 step: fold 32 logits of one query row (raw dot products; invisible
-// entries -inf) into its running (m, Z), m and the exponents in log2 units
-// scaled by sl = scale * log2(e), Z = sum 2^(x*sl - m).  m is a reference
-// point, not the running maximum: the exponentials are taken against the
-// current m, and only a chunk whose sum leaves [0, 2^20] (a term above about
-// 2^15, an overflow, or the first visible chunk, where m is -inf and the sum
-// is inf or NaN) takes the slow step that moves m to the chunk maximum and
-// rescales Z.  m + log2 Z is the same either way.
-__device__ __forceinline__ void online_update32(const float (&v)[32], float sl, float& m, float& z) {
-  const float s = exp_sum32(v, sl, m);
-  if (s <= 1048576.f) {
-    z += s;
-    return;
-  }
-  const float mx = max32(v) * sl;
-  if (mx == -INFINITY) return;        // nothing visible in this chunk
-  const float mn = fmaxf(m, mx);
-  z = z * ex2_approx(m - mn) + exp_sum32(v, sl, mn);
-  m = mn;
-}
-
 __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   float4 r;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "r"(addr));
   return r;
+}
+
+// Pass 1 folds the logits of one query row (raw dot products; invisible
+// entries -inf) into its running (m, Z), m and the exponents in log2 units
+// scaled by sl = scale * log2(e), Z = sum 2^(x*sl - m).  m is a reference
+// point, not the running maximum: the exponentials are taken against the
+// current m, and only a unit whose chunk sums leave [0, 2^20] (a term above
+// about 2^15, an overflow, or the first visible chunk, where m is -inf and a
+// sum is inf or NaN) takes this slow step, which moves m to the maximum of the
+// unit's CPW chunks (if above m) and rescales Z.  m + log2 Z is the same
+// either way.
+template <int CPW>
+__device__ __forceinline__ void online_rescale(const float (&va)[32], const float (&vb)[32], float sl, float& m,
+                                               float& z) {
+  const float mx = (CPW == 2 ? fmaxf(max32(va), max32(vb)) : max32(va)) * sl;
+  if (mx == -INFINITY) return;        // nothing visible
+  const float mn = fmaxf(m, mx);
+  float sum = exp_sum32(va, sl, mn);
+  if (CPW == 2) sum += exp_sum32(vb, sl, mn);
+  z = z * ex2_approx(m - mn) + sum;
+  m = mn;
 }
 
 // Pass-2 step, unmasked: acc += 2^(v * sl - lse2) over 32 query columns of one
@@ -329,28 +329,6 @@ __device__ __forceinline__ bool wait_slot_fast(const ScoreArgs& a, const Smem& s
     return true;
   }
   return wait_slot(a, sm, slot, parity);
-}
-
-// This warp's share of a unit: CPW chunks of 32 columns at taddr, taddr +
-// step, ... (TMEM lane quarter and slot already in taddr).  Both loads are
-// issued before the first reduction; the slot is released once the last
-// load has landed, before the last reduction.  process(v, c) gets chunk c.
-template <int CPW, class F>
-__device__ __forceinline__ void drain(uint32_t taddr, uint32_t step, const Smem& sm, int slot, int lane, F&& process) {
-  static_assert(CPW == 1 || CPW == 2, "one or two chunks per warp and unit");
-  float va[32], vb[32];
-  tmem_ld32(taddr, va);
-  tmem_wait_ld();
-  if (CPW == 2) {
-    tmem_ld32(taddr + step, vb);
-    process(va, 0);
-    tmem_wait_ld();
-    release_slot(sm, slot, lane);
-    process(vb, 1);
-  } else {
-    release_slot(sm, slot, lane);
-    process(va, 0);
-  }
 }
 
 // --------------------------------------------------- producer and MMA -----
@@ -528,14 +506,29 @@ __device__ __forceinline__ void pass1_epilogue(const ScoreArgs& a, const Smem& s
       float zh = h == 0 ? z0 : h == 1 ? z1 : h == 2 ? z2 : z3;
       const bool live = lh != INT_MIN;
       const int lim = live ? lh - kt : 0;   // this warp's columns j > lim are invisible
-      drain<CPW>(tbase + uint32_t(slot * geo.slot_cols), 32u, sm, slot, lane, [&](float (&v)[32], int c) {
-        if (masked) {
+      // Both chunks are loaded before one wait, the slot is released, then the
+      // two chunk sums are formed independently with one overflow check (a
+      // per-chunk check would make each chunk's exponentials wait on the
+      // previous sum).
+      float va[32], vb[32];
+      const uint32_t ta = tbase + uint32_t(slot * geo.slot_cols);
+      tmem_ld32(ta, va);
+      if (CPW == 2) tmem_ld32(ta + 32u, vb);
+      tmem_wait_ld();
+      release_slot(sm, slot, lane);
+      if (masked) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (32 * c + j > lim) v[j] = -INFINITY;
+        for (int j = 0; j < 32; ++j) {
+          if (j > lim) va[j] = -INFINITY;
+          if (CPW == 2 && 32 + j > lim) vb[j] = -INFINITY;
         }
-        if (live) online_update32(v, sl, mh, zh);
-      });
+      }
+      if (live) {
+        const float sa = exp_sum32(va, sl, mh);
+        const float sb = CPW == 2 ? exp_sum32(vb, sl, mh) : 0.f;
+        if (sa <= 1048576.f && sb <= 1048576.f) zh += sa + sb;
+        else online_rescale<CPW>(va, vb, sl, mh, zh);
+      }
       if (h == 0) { m0 = mh; z0 = zh; }
       else if (h == 1) { m1 = mh; z1 = zh; }
       else if (h == 2) { m2 = mh; z2 = zh; }
@@ -648,11 +641,22 @@ __device__ __forceinline__ void pass2_epilogue(const ScoreArgs& a, const Smem& s
         if (kprev < k1) out[kprev] = red_sum(sm.red, i - lag, krow);
       }
       const int col0 = u * geo.unit_cols + cb * 32;
-      drain<CPW>(tq + uint32_t(slot * 256), uint32_t(32 * kW), sm, slot, lane, [&](float (&v)[32], int c) {
-        const int col = col0 + c * 32 * kW;
-        if (!masked) normalised_sum32(v, nlse_s + 4 * col, sl, acc0, acc1);
-        else acc0 = add2(acc0, pack2(normalised_sum32_masked(v, sm.nlse + col, sm.tq + col, key, sl), 0.f));
-      });
+      {   // both chunks loaded, one wait, the slot released, then the math
+        float va[32], vb[32];
+        const uint32_t ta = tq + uint32_t(slot * 256);
+        tmem_ld32(ta, va);
+        if (CPW == 2) tmem_ld32(ta + uint32_t(32 * kW), vb);
+        tmem_wait_ld();
+        release_slot(sm, slot, lane);
+        if (!masked) {
+          normalised_sum32(va, nlse_s + 4 * col0, sl, acc0, acc1);
+          if (CPW == 2) normalised_sum32(vb, nlse_s + 4 * (col0 + 32 * kW), sl, acc0, acc1);
+        } else {
+          float t = normalised_sum32_masked(va, sm.nlse + col0, sm.tq + col0, key, sl);
+          if (CPW == 2) t += normalised_sum32_masked(vb, sm.nlse + col0 + 32 * kW, sm.tq + col0 + 32 * kW, key, sl);
+          acc0 = add2(acc0, pack2(t, 0.f));
+        }
+      }
     }
     if (!ok) break;
     float lo, hi;
