@@ -98,9 +98,15 @@ typedef struct upf_params {
  * rows are written.  Pointer pairs marked "nullable pair" may both be NULL.
  * row_bytes:      bytes of one hidden-state row (multiple of 16; e.g. 2*hidden
  *                 for bf16), both hidden pointers 16-byte aligned.
- * hidden_in/out:  device [T, row_bytes] / [T, row_bytes] (nullable pair).
- * pos_in/out:     device int64 [T] position ids (nullable pair).
- * slot_in/out:    device int64 [T] KV-cache slot ids (nullable pair).
+ * hidden_in/out:  [T, row_bytes] / [T, row_bytes] (nullable pair).
+ * pos_in/out:     int64 [T] position ids (nullable pair).
+ * slot_in/out:    int64 [T] KV-cache slot ids (nullable pair).
+ *                 These six may be device memory or host memory the device
+ *                 reads and writes directly (page-locked host memory under
+ *                 unified addressing, or any host memory where the device has
+ *                 pageable-memory access): the gather then moves only the kept
+ *                 rows across the host link.  Other host pointers are
+ *                 rejected with UPF_ERR_INVALID_ARG.
  * kept_index:     device int32 [T]: packed input index of each kept row (nullable).
  * cu_seqlens_out: device int32 [R+1]: packed offsets of the compacted batch.
  * total_kept:     device int32 [1]: cu_seqlens_out[R].

@@ -271,7 +271,30 @@ upf_status check_score_io(const Plan& pl, const void* q, int64_t qs, const void*
   return UPF_OK;
 }
 
-upf_status check_compact_io(const Plan& pl, const uint32_t* keep_bits, const upf_compact_io* io) {
+// A compaction buffer the kernels may dereference: device or managed memory,
+// page-locked host memory mapped at the same address (unified addressing), or
+// any host memory when the device reads pageable memory itself.
+bool device_accessible(const void* p, int device) {
+  if (!p) return true;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+      return true;
+    case cudaMemoryTypeHost:
+      return at.devicePointer == p;
+    default: {
+      int pageable = 0;
+      return cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, device) == cudaSuccess && pageable;
+    }
+  }
+}
+
+upf_status check_compact_io(const Plan& pl, const uint32_t* keep_bits, const upf_compact_io* io, int device) {
   if (!keep_bits) return fail(UPF_ERR_INVALID_ARG, "keep_bits is NULL");
   if (!io) return fail(UPF_ERR_INVALID_ARG, "compact io is NULL");
   if (!io->cu_seqlens_out || !io->total_kept) return fail(UPF_ERR_INVALID_ARG, "cu_seqlens_out and total_kept are required");
@@ -283,6 +306,11 @@ upf_status check_compact_io(const Plan& pl, const uint32_t* keep_bits, const upf
     if (!aligned16(io->hidden_in) || !aligned16(io->hidden_out))
       return fail(UPF_ERR_INVALID_ARG, "hidden buffers must be 16-byte aligned");
   }
+  const void* bufs[6] = {io->hidden_in, io->hidden_out, io->pos_in, io->pos_out, io->slot_in, io->slot_out};
+  static const char* names[6] = {"hidden_in", "hidden_out", "pos_in", "pos_out", "slot_in", "slot_out"};
+  for (int i = 0; i < 6; ++i)
+    if (!device_accessible(bufs[i], device))
+      return fail(UPF_ERR_INVALID_ARG, "%s is host memory the device cannot access (use page-locked memory)", names[i]);
   if (!io->history != !io->history_len) return fail(UPF_ERR_INVALID_ARG, "history/history_len must both be set or both NULL");
   if (io->history && io->history_cap < 1) return fail(UPF_ERR_INVALID_ARG, "history_cap must be >= 1");
   (void)pl;
@@ -623,7 +651,7 @@ upf_status upf_compact(upf_ctx* ctx, const upf_batch* batch, const uint32_t* kee
   Plan pl;
   if ((st = make_plan(ctx, batch, nullptr, false, &pl)) != UPF_OK) return st;
   if ((st = check_ws(pl, ws, ws_bytes)) != UPF_OK) return st;
-  if ((st = check_compact_io(pl, keep_bits, io)) != UPF_OK) return st;
+  if ((st = check_compact_io(pl, keep_bits, io, ctx->device)) != UPF_OK) return st;
   DeviceGuard guard(ctx->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return launch_compact_all(ctx, compact_args(ctx, batch, pl, keep_bits, io, ws), s, false);
@@ -682,7 +710,7 @@ upf_status upf_select_tokens(upf_ctx* ctx, const upf_batch* batch, const upf_par
   if ((st = check_ws(pl, ws, ws_bytes)) != UPF_OK) return st;
   if ((st = check_score_io(pl, q, q_row_stride, k, k_row_stride)) != UPF_OK) return st;
   if (!keep_bits || !kept_count) return fail(UPF_ERR_INVALID_ARG, "keep_bits and kept_count are required");
-  if ((st = check_compact_io(pl, keep_bits, io)) != UPF_OK) return st;
+  if ((st = check_compact_io(pl, keep_bits, io, ctx->device)) != UPF_OK) return st;
   DeviceGuard guard(ctx->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const upf::DescribeArgs da = describe_args(ctx, batch, pl, ws);

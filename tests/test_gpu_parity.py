@@ -117,6 +117,10 @@ SMALL = [
     ("gemma-n32-G128", dict(lengths=[2000, 640], H=(16, 8, 256), hidden=3840, n=32, G=128, planted=[2, 1])),
     ("tail-only", dict(lengths=[100, 129, 257], H=(8, 2, 128), hidden=256, n=128, G=64, planted=[0, 0, 0])),
     ("odd-hidden", dict(lengths=[3333], H=(8, 1, 128), hidden=520, n=64, G=16, planted=[7])),
+    # 384 query rows per chunk: pass-2 units of 128 columns, three per key tile
+    ("gqa3-rows384", dict(lengths=[2600, 1500], H=(6, 2, 128), hidden=256, n=128, G=64, planted=[3, 2])),
+    # 64 query rows: one unit per key tile in both passes
+    ("rows64-d128", dict(lengths=[3100, 900, 2049], H=(8, 4, 128), hidden=256, n=32, G=32, planted=[2, 1, 1])),
 ]
 
 
@@ -401,3 +405,59 @@ def test_select_large_request_many_blocks(sel):
     assert status == 0
     bad = C.self_consistency_mismatches(mask, bs, [0, nb * G], G, 0.95, 128, 128)
     assert not bad, bad[:5]
+
+
+def test_compaction_with_host_buffers(sel):
+    """Hidden rows, positions and slots in page-locked host memory (read and
+    written by the gather over the host link) give the device buffers' results."""
+    spec = small_spec("hostbuf", SMALL[1][1])
+    w = wl.generate(spec)
+    p = params_of(spec)
+    dev_out, status, _ = run_gpu(sel, w, p)
+    assert status == 0
+    q = _up(w.q_full_bits().view(np.int16)).view(torch.bfloat16)
+    k = _up(w.k_bits.view(np.int16)).view(torch.bfloat16)
+    hid_h = torch.from_numpy(w.hidden_bits().view(np.int16)).pin_memory()
+    pos_h = torch.from_numpy(w.positions()).pin_memory()
+    slot_h = torch.from_numpy(w.slots()).pin_memory()
+    out = sel.alloc_outputs(w.cu_seqlens, spec.block)
+    out.hidden_out = torch.empty_like(hid_h).pin_memory()
+    out.pos_out = torch.empty_like(pos_h).pin_memory()
+    out.slot_out = torch.empty_like(slot_h).pin_memory()
+    s = w.spec
+    sel.select_tokens(q, k, w.cu_seqlens, _up(w.cu_seqlens), s.num_q_heads, s.num_kv_heads, s.head_dim, hid_h,
+                      pos_h, slot_h, params=p, kv_of_q=s.kv_of_q, out=out)
+    torch.cuda.synchronize()
+    assert sel.status() == 0
+    total = int(out.total_kept.item())
+    assert total == int(dev_out.total_kept.item())
+    assert torch.equal(out.keep_bits, dev_out.keep_bits)
+    assert torch.equal(out.hidden_out[:total], dev_out.hidden_out[:total].cpu())
+    assert torch.equal(out.pos_out[:total], dev_out.pos_out[:total].cpu())
+    assert torch.equal(out.slot_out[:total], dev_out.slot_out[:total].cpu())
+
+
+def test_compaction_pageable_host_memory_is_refused_or_exact(sel):
+    """An ordinary (pageable) host buffer is refused with a clear error, unless
+    the device reads pageable host memory itself; then the rows are exact."""
+    spec = small_spec("pageable", SMALL[4][1])
+    w = wl.generate(spec)
+    p = params_of(spec)
+    dev_out, status, _ = run_gpu(sel, w, p)
+    assert status == 0
+    q = _up(w.q_full_bits().view(np.int16)).view(torch.bfloat16)
+    k = _up(w.k_bits.view(np.int16)).view(torch.bfloat16)
+    hid = torch.from_numpy(w.hidden_bits().view(np.int16)).clone()   # pageable host memory
+    out = sel.alloc_outputs(w.cu_seqlens, spec.block)
+    out.hidden_out = torch.empty(hid.shape, dtype=hid.dtype, device=DEV)
+    s = w.spec
+    try:
+        sel.select_tokens(q, k, w.cu_seqlens, _up(w.cu_seqlens), s.num_q_heads, s.num_kv_heads, s.head_dim, hid,
+                          params=p, kv_of_q=s.kv_of_q, out=out)
+        torch.cuda.synchronize()
+    except B.UpfError as e:
+        assert "cannot access" in str(e)
+        return
+    assert sel.status() == 0
+    total = int(out.total_kept.item())
+    assert torch.equal(out.hidden_out[:total], dev_out.hidden_out[:total])
