@@ -58,6 +58,7 @@ def parse_args():
     ap.add_argument("--top-p", type=float, default=None, help="override p (e.g. 1.0 keeps every token)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-gather-p1", action="store_true", help="skip the supplementary all-kept gather point")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
     return ap.parse_args()
@@ -432,6 +433,11 @@ def main():
         e2e = run_e2e(args, torch, sel, spec, w, cu, params, q_dev, k_dev, hid_dev, pos_dev, slot_dev, cu_dev, out,
                       dev, world)
 
+    # supplementary gather point: the mask all ones (p = 1), full traffic
+    gather_p1 = None
+    if not args.no_gather_p1:
+        gather_p1 = run_gather_p1(torch, sel, spec, w, cu, cu_dev, hid_dev, pos_dev, slot_dev, out, peaks)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
@@ -444,13 +450,51 @@ def main():
                 "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms),
                             "traced_mean": statistics.mean(traced), "stage_sum": sum(stage_ms) / args.steps},
                 "kept_tokens": kept_total, "kept_fraction": kept_total / T,
-                "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e, "gather_p1": gather_p1,
                 "gpu_launches": int(sum(launches)), "clocks": clk, "wall_s": wall}
         print(json.dumps(line), flush=True)
     sel.close()
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def run_gather_p1(torch, sel, spec, w, cu, cu_dev, hid_dev, pos_dev, slot_dev, out, peaks, launches=5):
+    """The compaction with every token kept (upf_compact with an all-ones mask on
+    the same batch): the gather kernel then moves 2 T (row_bytes + 16) bytes, far
+    more than L2, so its time is the HBM bound of the compaction at full traffic."""
+    from sparse_long_context_tail_gb300 import _binding as B
+    T = w.total_tokens
+    row_bytes = hid_dev.stride(0) * hid_dev.element_size()
+    bits = torch.full(((T + 31) // 32,), -1, dtype=torch.int32, device=hid_dev.device)
+    batch, keep = B.make_batch(cu_dev.data_ptr(), cu, spec.num_q_heads, spec.num_kv_heads, spec.head_dim)
+    nbytes = B.upf_workspace_bytes(batch, B.make_params())
+    ws = sel.workspace(nbytes)
+    io = B.make_compact_io(row_bytes=row_bytes, hidden_in=hid_dev.data_ptr(), hidden_out=out.hidden_out.data_ptr(),
+                           pos_in=pos_dev.data_ptr(), pos_out=out.pos_out.data_ptr(), slot_in=slot_dev.data_ptr(),
+                           slot_out=out.slot_out.data_ptr(), kept_index=out.kept_index.data_ptr(),
+                           cu_seqlens_out=out.cu_seqlens_out.data_ptr(), total_kept=out.total_kept.data_ptr())
+    stream = torch.cuda.current_stream().cuda_stream
+    B.upf_compact(sel.ctx, batch, bits.data_ptr(), io, ws.data_ptr(), ws.numel(), stream)   # warm-up
+    torch.cuda.synchronize()
+    B.upf_profile_read(sel.ctx)
+    B.upf_profile_enable(sel.ctx, True)
+    for _ in range(launches):
+        B.upf_compact(sel.ctx, batch, bits.data_ptr(), io, ws.data_ptr(), ws.numel(), stream)
+    torch.cuda.synchronize()
+    n_l, ms = B.upf_profile_read(sel.ctx)
+    B.upf_profile_enable(sel.ctx, False)
+    kept = int(out.total_kept.item())
+    assert kept == T, (kept, T)
+    gi = STAGES.index("compact_gather")
+    per = ms[gi] / max(1, n_l[gi])
+    moved = 2 * T * (row_bytes + 16)
+    gbs = moved / (per / 1e3) / 1e9
+    del keep
+    return {"kept_tokens": kept, "bytes_per_launch": moved, "gather_ms_per_launch": per, "achieved_gbs": gbs,
+            "peak_gbs": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
+            "compaction_ms_per_launch": sum(ms[STAGES.index(k)] for k in ("compact_count", "compact_index",
+                                                                         "compact_gather")) / launches}
 
 
 def run_e2e(args, torch, sel, spec, w, cu, params, q_dev, k_dev, hid_dev, pos_dev, slot_dev, cu_dev, out, dev, world):
