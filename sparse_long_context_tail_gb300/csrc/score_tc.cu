@@ -706,15 +706,28 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       int t = -1;
       if (row < rows_c) {
         t = it.L - a.n + (it.qc * a.QC + row) % a.n;
-        float mm = -INFINITY;
-        for (int s = 0; s < nsplit1; ++s)
-          mm = fmaxf(mm, a.p1part[item_index(a.item_off1, it.r, it.g, s, it.qc, nsplit1, a.NQC) * a.QC + row].x);
-        float Z = 0.f;
-        if (mm > -INFINITY)
-          for (int s = 0; s < nsplit1; ++s) {
-            const float2 p = a.p1part[item_index(a.item_off1, it.r, it.g, s, it.qc, nsplit1, a.NQC) * a.QC + row];
-            if (p.y > 0.f) Z += p.y * exp2f(p.x - mm);
+        // One online merge over the key splits, sixteen partials loaded
+        // before any is used: a load feeding each step would expose one L2
+        // latency per split while the MMA waits for the first unit's reader.
+        const float2* src = a.p1part + item_index(a.item_off1, it.r, it.g, 0, it.qc, nsplit1, a.NQC) * a.QC + row;
+        const int64_t split_stride = (int64_t)a.NQC * a.QC;   // consecutive splits of one (g, qc)
+        float mm = -INFINITY, Z = 0.f;
+        for (int s0 = 0; s0 < nsplit1; s0 += 16) {
+          float2 pp[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            pp[k] = s0 + k < nsplit1 ? src[(s0 + k) * split_stride] : make_float2(-INFINITY, 0.f);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            if (!(pp[k].y > 0.f)) continue;
+            if (pp[k].x > mm) {
+              Z = Z * exp2f(mm - pp[k].x) + pp[k].y;
+              mm = pp[k].x;
+            } else {
+              Z += pp[k].y * exp2f(pp[k].x - mm);
+            }
           }
+        }
         if (Z > 0.f && t >= 0) l2 = mm + log2f(Z);
         else t = -1;
       }
