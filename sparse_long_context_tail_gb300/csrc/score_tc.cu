@@ -56,7 +56,8 @@ constexpr int kThreadsTC = kEpiThreads + 64;   // 576
 constexpr int kStageBytes = 32768;             // largest ring stage
 constexpr int kMaxStages = 8;
 constexpr int kMaxSlots = 4;
-constexpr int kRedTiles = 8;                   // pass 2: tiles of per-key sums in flight
+constexpr int kRedTiles = 8;
+constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxSlots + 3;   // + qfull, fin, decide                   // pass 2: tiles of per-key sums in flight
 constexpr int kSmemLimit = 232448;             // opt-in dynamic shared memory per CTA
 constexpr long long kWaitLimit = 4000000000LL; // clock cycles (about 2 s)
 constexpr uint32_t kIdleNs = 4000;              // longest suspension of a waiting role per poll
@@ -99,7 +100,7 @@ __host__ __device__ inline Geo geometry(int pass, int d, int QC) {
   g.q_bytes = g.S * QC * 128;
   g.extra_bytes = pass == 2 ? 8 * QC + kRedTiles * kW * 128 * 4 : 0;
   const int fixed = 1024 /* alignment slack */ + g.q_bytes + g.extra_bytes +
-                    8 * (2 * kMaxStages + 2 * kMaxSlots + 2) + 16;
+                    8 * kNumBars + 16;
   g.NS = imin(kMaxStages, (kSmemLimit - fixed) / g.stage_bytes);
   g.smem = fixed + g.NS * g.stage_bytes;
   return g;
@@ -112,9 +113,10 @@ struct Smem {
   float* nlse;            // pass 2: -lse2 per chunk row (+inf rows: -inf)
   int* tq;                // pass 2: query position per chunk row (-1: none)
   float* red;             // pass 2: [kRedTiles][kW][128] per-key sums of the column quarters
-  uint64_t* bars;         // full[8], empty[8], tfull[4], tempty[4], qfull, fin
+  uint64_t* bars;         // full[8], empty[8], tfull[4], tempty[4], qfull, fin, decide
   uint32_t* tmem_slot;
   int* abort_flag;
+  int* redo;              // pass 1: run the item again on the checked path
 };
 
 __device__ __forceinline__ Smem carve(unsigned char* raw, const Geo& g, int QC) {
@@ -129,9 +131,10 @@ __device__ __forceinline__ Smem carve(unsigned char* raw, const Geo& g, int QC) 
   s.red = reinterpret_cast<float*>(p + 8 * QC);
   p += g.extra_bytes;
   s.bars = reinterpret_cast<uint64_t*>(p);
-  p += 8 * (2 * kMaxStages + 2 * kMaxSlots + 2);
+  p += 8 * kNumBars;
   s.tmem_slot = reinterpret_cast<uint32_t*>(p);
   s.abort_flag = reinterpret_cast<int*>(p + 8);
+  s.redo = reinterpret_cast<int*>(p + 12);
   return s;
 }
 
@@ -147,6 +150,10 @@ __device__ __forceinline__ uint32_t bar_qfull(const Smem& sm) {
 __device__ __forceinline__ uint32_t bar_fin(const Smem& sm) {
   return smem_u32(&sm.bars[2 * kMaxStages + 2 * kMaxSlots + 1]);
 }
+// Pass 1: the epilogue's verdict after the fast pass over an item (one arrival).
+__device__ __forceinline__ uint32_t bar_decide(const Smem& sm) {
+  return smem_u32(&sm.bars[2 * kMaxStages + 2 * kMaxSlots + 2]);
+}
 
 __device__ __forceinline__ void init_barriers(const Smem& sm) {
   for (int i = 0; i < kMaxStages; ++i) {
@@ -159,7 +166,9 @@ __device__ __forceinline__ void init_barriers(const Smem& sm) {
   }
   mbar_init(bar_qfull(sm), 1);
   mbar_init(bar_fin(sm), 1);
+  mbar_init(bar_decide(sm), 1);
   *sm.abort_flag = 0;
+  *sm.redo = 0;
   fence_barrier_init();
 }
 
@@ -333,10 +342,11 @@ __device__ __forceinline__ bool wait_slot_fast(const ScoreArgs& a, const Smem& s
 
 // --------------------------------------------------- producer and MMA -----
 
-// Producer: the query chunk (once), then every key tile stage by stage.
-// Returns the number of stage loads issued.
+// Producer: the query chunk (once), then every key tile stage by stage
+// (pass 1: a second time when the epilogue's verdict asks for it).  Returns
+// the number of stage loads issued.
 __device__ int produce(const ScoreArgs& a, const CUtensorMap* tq_map, const CUtensorMap* tk_map, const Smem& sm,
-                       const Geo& geo, const ItemTC& it, int rows_c, int k0, int ntiles) {
+                       const Geo& geo, const ItemTC& it, int rows_c, int k0, int ntiles, bool may_repeat) {
   const int BQ = a.q_box_rows;
   const int boxes = rows_c / BQ;
   mbar_arrive_expect_tx(bar_qfull(sm), uint32_t(boxes) * geo.S * BQ * 128);
@@ -349,20 +359,31 @@ __device__ int produce(const ScoreArgs& a, const CUtensorMap* tq_map, const CUte
                   bar_qfull(sm));
   }
   const int total = ntiles * geo.spt;
-  int q = 0, st = 0, part = 0, key = it.tok0 + k0;
+  int q = 0, st = 0;
   uint32_t ph = 0;
-  for (; q < total; ++q) {
-    if (aborted(sm)) break;
-    if (!mbar_wait_idle(bar_empty(sm, st), ph ^ 1u, kWaitLimit, kIdleNs)) {
-      abort_with_timeout(a, sm);
-      break;
+  for (int round = 0; round < (may_repeat ? 2 : 1); ++round) {
+    if (round == 1) {   // pass 1: the tiles again only if the epilogue asks for it
+      if (!mbar_wait_idle(bar_decide(sm), 0, kWaitLimit, kIdleNs)) {
+        abort_with_timeout(a, sm);
+        break;
+      }
+      if (*reinterpret_cast<volatile int*>(sm.redo) == 0) break;
     }
-    mbar_arrive_expect_tx(bar_full(sm, st), uint32_t(geo.stage_bytes));
-    const uint32_t dst = smem_u32(sm.ring) + uint32_t(st * geo.stage_bytes);
-    for (int ss = 0; ss < geo.sps; ++ss)
-      tma_load_3d(dst + uint32_t(ss * geo.slice_bytes), tk_map, (part * geo.sps + ss) * 64, it.g, key, bar_full(sm, st));
-    if (++st == geo.NS) { st = 0; ph ^= 1u; }
-    if (++part == geo.spt) { part = 0; key += geo.tile_keys; }
+    int part = 0, key = it.tok0 + k0;
+    for (int n = 0; n < total; ++n, ++q) {
+      if (aborted(sm)) return q;
+      if (!mbar_wait_idle(bar_empty(sm, st), ph ^ 1u, kWaitLimit, kIdleNs)) {
+        abort_with_timeout(a, sm);
+        return q;
+      }
+      mbar_arrive_expect_tx(bar_full(sm, st), uint32_t(geo.stage_bytes));
+      const uint32_t dst = smem_u32(sm.ring) + uint32_t(st * geo.stage_bytes);
+      for (int ss = 0; ss < geo.sps; ++ss)
+        tma_load_3d(dst + uint32_t(ss * geo.slice_bytes), tk_map, (part * geo.sps + ss) * 64, it.g, key,
+                    bar_full(sm, st));
+      if (++st == geo.NS) { st = 0; ph ^= 1u; }
+      if (++part == geo.spt) { part = 0; key += geo.tile_keys; }
+    }
   }
   return q;
 }
@@ -383,7 +404,7 @@ __device__ void drain_loads(const Smem& sm, const Geo& geo, int issued) {
 // query columns [W u, W u + W) (B, N = W = unit_cols).  Before returning it waits for all of
 // them to finish.
 __device__ void issue_mma(const ScoreArgs& a, const Smem& sm, const Geo& geo, int ntiles, int units, uint32_t tmem,
-                          bool keys_as_m) {
+                          bool keys_as_m, bool may_repeat) {
   // Division-free bookkeeping: this thread shares its scheduler with busy
   // epilogue warps, so every instruction between two MMAs costs issue slots.
   const uint32_t idesc = idesc_bf16_f32(128, uint32_t(geo.unit_cols));
@@ -395,6 +416,11 @@ __device__ void issue_mma(const ScoreArgs& a, const Smem& sm, const Geo& geo, in
   uint32_t ph = 0;       // its phase parity
   int slot = 0;          // TMEM slot of the next unit
   uint32_t sph = 0;      // its phase parity
+  for (int round = 0; ok && round < (may_repeat ? 2 : 1); ++round) {
+  if (round == 1) {        // pass 1: the tiles again only if the epilogue asks for it
+    ok = mbar_wait_idle(bar_decide(sm), 0, kWaitLimit, kIdleNs);
+    if (!ok || *reinterpret_cast<volatile int*>(sm.redo) == 0) break;
+  }
   for (int i = 0; ok && i < ntiles; ++i) {
     // A tile takes spt <= 2 consecutive ring stages; slice s lives in stage
     // part s / sps at offset (s % sps) slices, sps in {1, 2}.
@@ -428,6 +454,7 @@ __device__ void issue_mma(const ScoreArgs& a, const Smem& sm, const Geo& geo, in
     if (!ok) break;
     mma_commit(bar_empty(sm, st0));
     if (geo.spt == 2) mma_commit(bar_empty(sm, st1));
+  }
   }
   if (!ok) abort_with_timeout(a, sm);
   // Every MMA this thread issued must be done before TMEM can be freed.
@@ -466,10 +493,40 @@ __device__ __forceinline__ float red_sum(const float* red, int i, int krow) {
 
 // ------------------------------------------------------------- pass 1 -----
 
+template <bool B>
+struct Flag {
+  static constexpr bool value = B;
+};
+
+// OR of a predicate over the epilogue warps (named barrier 1 with reduction).
+__device__ __forceinline__ int epi_bar_or(int v) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, %2, q;\n\t"
+      "selp.s32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(v), "r"(kEpiThreads)
+      : "memory");
+  return r;
+}
+
 // Epilogue of pass 1.  This thread is row 128h + 32qd + lane of every unit h
 // and covers the column quarter cb of it (CPW chunks of 32 keys); it keeps
-// (m, Z) of up to four rows in registers.  At the end the quarters of every row are merged
-// through shared memory and one (m, Z) per row is stored.
+// (m, Z) of up to four rows in registers.  At the end the quarters of every
+// row are merged through shared memory and one (m, Z) per row is stored.
+//
+// An item is swept once on a fast path: the first key tile sets every row's
+// reference m to its maximum, later tiles add their exponential sums with no
+// test in the way (a test per unit made each unit's sums stall the warp) and
+// only note, in a flag, a sum that is not finite (a logit more than about 127
+// above the first tile's maximum).  Rows whose m is still -inf after the first
+// tile see no key of the item at all (keys are visible up to a position, and
+// the first tile holds the item's lowest keys) and are skipped.  If any row of
+// the CTA was flagged, the epilogue says so through the decide barrier and
+// the producer, the MMA and the epilogue sweep the item again on the checked
+// path, which moves m whenever a unit's sums leave [0, 2^20].
 template <int CPW>
 __device__ __forceinline__ void pass1_epilogue(const ScoreArgs& a, const Smem& sm, const Geo& geo, const ItemTC& it,
                                                int item, int rows_c, int MT, int k0, int ntiles, uint32_t tmem,
@@ -485,58 +542,77 @@ __device__ __forceinline__ void pass1_epilogue(const ScoreArgs& a, const Smem& s
     return (h < MT && row < rows_c) ? it.L - a.n + (it.qc * a.QC + row) % a.n - cb * span : INT_MIN;
   };
   const int l0 = lim_of(0), l1 = lim_of(1), l2 = lim_of(2), l3 = lim_of(3);
-  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-  float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+  float m0, m1, m2, m3, z0, z1, z2, z3;
   const uint32_t tbase = tmem + (uint32_t(qd * 32) << 16) + uint32_t(cb * span);
   bool ok = true;
   int uidx = 0;
-  for (int i = 0; ok && i < ntiles; ++i) {
-    const int kt = k0 + i * geo.tile_keys;   // request-relative first key of the tile
-    const bool masked = kt + geo.tile_keys - 1 > it.L - a.n;
+  auto sweep = [&](auto checked_flag) -> bool {   // returns: some sum not finite (fast path only)
+    constexpr bool kChecked = decltype(checked_flag)::value;
+    m0 = m1 = m2 = m3 = -INFINITY;
+    z0 = z1 = z2 = z3 = 0.f;
+    bool bad = false;
+    for (int i = 0; ok && i < ntiles; ++i) {
+      const int kt = k0 + i * geo.tile_keys;   // request-relative first key of the tile
+      const bool masked = kt + geo.tile_keys - 1 > it.L - a.n;
 #pragma unroll
-    for (int h = 0; h < 4; ++h, ++uidx) {
-      if (h >= MT) break;
-      const int slot = uidx % geo.nslots;
-      if (!wait_slot_fast(a, sm, slot, (uidx / geo.nslots) & 1)) {
-        ok = false;
-        break;
-      }
-      const int lh = h == 0 ? l0 : h == 1 ? l1 : h == 2 ? l2 : l3;
-      float mh = h == 0 ? m0 : h == 1 ? m1 : h == 2 ? m2 : m3;
-      float zh = h == 0 ? z0 : h == 1 ? z1 : h == 2 ? z2 : z3;
-      const bool live = lh != INT_MIN;
-      const int lim = live ? lh - kt : 0;   // this warp's columns j > lim are invisible
-      // Both chunks are loaded before one wait, the slot is released, then the
-      // two chunk sums are formed independently with one overflow check (a
-      // per-chunk check would make each chunk's exponentials wait on the
-      // previous sum).
-      float va[32], vb[32];
-      const uint32_t ta = tbase + uint32_t(slot * geo.slot_cols);
-      tmem_ld32(ta, va);
-      if (CPW == 2) tmem_ld32(ta + 32u, vb);
-      tmem_wait_ld();
-      release_slot(sm, slot, lane);
-      if (masked) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (j > lim) va[j] = -INFINITY;
-          if (CPW == 2 && 32 + j > lim) vb[j] = -INFINITY;
+      for (int h = 0; h < 4; ++h, ++uidx) {
+        if (h >= MT) break;
+        const int slot = uidx % geo.nslots;
+        if (!wait_slot_fast(a, sm, slot, (uidx / geo.nslots) & 1)) {
+          ok = false;
+          break;
         }
+        const int lh = h == 0 ? l0 : h == 1 ? l1 : h == 2 ? l2 : l3;
+        float mh = h == 0 ? m0 : h == 1 ? m1 : h == 2 ? m2 : m3;
+        float zh = h == 0 ? z0 : h == 1 ? z1 : h == 2 ? z2 : z3;
+        const bool live = lh != INT_MIN;
+        const int lim = live ? lh - kt : 0;   // this warp's columns j > lim are invisible
+        // Both chunks are loaded before one wait and the slot is released
+        // before the math.
+        float va[32], vb[32];
+        const uint32_t ta = tbase + uint32_t(slot * geo.slot_cols);
+        tmem_ld32(ta, va);
+        if (CPW == 2) tmem_ld32(ta + 32u, vb);
+        tmem_wait_ld();
+        release_slot(sm, slot, lane);
+        if (masked) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j > lim) va[j] = -INFINITY;
+            if (CPW == 2 && 32 + j > lim) vb[j] = -INFINITY;
+          }
+        }
+        if (live) {
+          if (kChecked) {
+            const float sa = exp_sum32(va, sl, mh);
+            const float sb = CPW == 2 ? exp_sum32(vb, sl, mh) : 0.f;
+            if (sa <= 1048576.f && sb <= 1048576.f) zh += sa + sb;
+            else online_rescale<CPW>(va, vb, sl, mh, zh);
+          } else if (i == 0) {
+            online_rescale<CPW>(va, vb, sl, mh, zh);   // the reference: the first tile's maximum
+          } else if (mh > -INFINITY) {
+            const float t = exp_sum32(va, sl, mh) + (CPW == 2 ? exp_sum32(vb, sl, mh) : 0.f);
+            zh += t;
+            bad |= !(t <= 3.0e38f);
+          }
+        }
+        if (h == 0) { m0 = mh; z0 = zh; }
+        else if (h == 1) { m1 = mh; z1 = zh; }
+        else if (h == 2) { m2 = mh; z2 = zh; }
+        else { m3 = mh; z3 = zh; }
       }
-      if (live) {
-        const float sa = exp_sum32(va, sl, mh);
-        const float sb = CPW == 2 ? exp_sum32(vb, sl, mh) : 0.f;
-        if (sa <= 1048576.f && sb <= 1048576.f) zh += sa + sb;
-        else online_rescale<CPW>(va, vb, sl, mh, zh);
-      }
-      if (h == 0) { m0 = mh; z0 = zh; }
-      else if (h == 1) { m1 = mh; z1 = zh; }
-      else if (h == 2) { m2 = mh; z2 = zh; }
-      else { m3 = mh; z3 = zh; }
     }
+    return bad || !(z0 <= 3.0e38f && z1 <= 3.0e38f && z2 <= 3.0e38f && z3 <= 3.0e38f);
+  };
+  const bool bad = sweep(Flag<false>{}) && ok;
+  const int redo = epi_bar_or(bad ? 1 : 0) && !aborted(sm);
+  if (threadIdx.x == 0) {
+    *reinterpret_cast<volatile int*>(sm.redo) = redo;
+    mbar_arrive(bar_decide(sm));
   }
+  if (redo) sweep(Flag<true>{});
   // The ring is idle here: every MMA, hence every load, finished before the
-  // last unit was read.
+  // last unit was read, and no second sweep follows.
   float2* red = reinterpret_cast<float2*>(sm.ring);   // [kW][QC]
   if (ok) {
     red[cb * a.QC + r0] = make_float2(m0, z0);
@@ -583,9 +659,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 
   int issued = 0;
   if (warp == kProducerWarp) {
-    if (lane == 0) issued = produce(a, &tq_map, &tk_map, sm, geo, it, rows_c, k0, ntiles);
+    if (lane == 0) issued = produce(a, &tq_map, &tk_map, sm, geo, it, rows_c, k0, ntiles, true);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) issue_mma(a, sm, geo, ntiles, MT, tmem, false);
+    if (lane == 0) issue_mma(a, sm, geo, ntiles, MT, tmem, false, true);
   } else if (geo.tile_keys / kW == 64) {
     pass1_epilogue<2>(a, sm, geo, it, item, rows_c, MT, k0, ntiles, tmem, warp, lane);
   } else {
@@ -692,9 +768,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 
   int issued = 0;
   if (warp == kProducerWarp) {
-    if (lane == 0) issued = produce(a, &tq_map, &tk_map, sm, geo, it, rows_c, k0, ntiles);
+    if (lane == 0) issued = produce(a, &tq_map, &tk_map, sm, geo, it, rows_c, k0, ntiles, false);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) issue_mma(a, sm, geo, ntiles, U, tmem, true);
+    if (lane == 0) issue_mma(a, sm, geo, ntiles, U, tmem, true, false);
   } else {
     // lse2 of every query row of the chunk from the pass-1 partials (all key
     // splits), stored negated; -inf marks rows that do not exist (padding,

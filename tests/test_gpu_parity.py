@@ -461,3 +461,28 @@ def test_compaction_pageable_host_memory_is_refused_or_exact(sel):
     assert sel.status() == 0
     total = int(out.total_kept.item())
     assert torch.equal(out.hidden_out[:total], dev_out.hidden_out[:total])
+
+
+def test_pass1_sweeps_again_after_a_huge_logit_jump(sel):
+    """One key with a logit about 2900 (log2 units) above every key of its
+    item's first tile overflows pass 1's fast-path sums; that item is swept
+    again on the checked path and every score still matches the oracle."""
+    L, Hq, Hkv, d, n = 40000, 2, 1, 64, 32       # key splits of 512 keys: two 256-key tiles per item
+    rng = np.random.default_rng(31)
+    q = (0.5 * rng.standard_normal((L, Hq, d))).astype(np.float32)
+    k = (0.5 * rng.standard_normal((L, Hkv, d))).astype(np.float32)
+    q[L - n:] = 4.0
+    big = 512 * 40 + 300                          # second tile of its item
+    k[big] = 64.0
+    q_bits, k_bits = wl.f32_to_bf16_bits(q), wl.f32_to_bf16_bits(k)
+    cu = np.array([0, L], dtype=np.int32)
+    p = B.make_params(n_tail=n, block=64, top_p=0.99)
+    qd = _up(q_bits.view(np.int16)).view(torch.bfloat16)
+    kd = _up(k_bits.view(np.int16)).view(torch.bfloat16)
+    out = sel.select_tokens(qd, kd, cu, _up(cu), Hq, Hkv, d, params=p)
+    torch.cuda.synchronize()
+    assert sel.status() == 0
+    ref = oracle.token_scores(k_bits, q_bits[L - n:], cu, Hq, Hkv, d, n)
+    got = out.scores.cpu().numpy()
+    assert C.score_violations(got, ref, cu)["ok"]
+    assert got[big] > 0.99
