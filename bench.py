@@ -58,6 +58,7 @@ def parse_args():
     ap.add_argument("--top-p", type=float, default=None, help="override p (e.g. 1.0 keeps every token)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip timing the step replayed from a CUDA graph")
     ap.add_argument("--no-gather-p1", action="store_true", help="skip the supplementary all-kept gather point")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
@@ -385,6 +386,11 @@ def main():
     traced = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     _, stage_ms = B.upf_profile_read(sel.ctx)
     B.upf_profile_enable(sel.ctx, False)
+    # The same step captured once in a CUDA graph and replayed (launches keep
+    # their programmatic-dependent-launch edges inside the graph).
+    graph = None
+    if not args.no_graph:
+        graph = graph_replay(torch, step, stream, args.steps, flush)
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
@@ -451,12 +457,42 @@ def main():
                             "traced_mean": statistics.mean(traced), "stage_sum": sum(stage_ms) / args.steps},
                 "kept_tokens": kept_total, "kept_fraction": kept_total / T,
                 "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e, "gather_p1": gather_p1,
+                "graph": graph,
                 "gpu_launches": int(sum(launches)), "clocks": clk, "wall_s": wall}
         print(json.dumps(line), flush=True)
     sel.close()
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def graph_replay(torch, step, stream, steps, flush):
+    """Capture one step in a CUDA graph and time `steps` replays (same inputs
+    and outputs; the L2 flush stays outside the graph, between replays)."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()                      # one eager step on the capture stream first
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=side):
+            step()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    cur = torch.cuda.current_stream()
+    for i in range(steps):
+        starts[i].record(cur)
+        g.replay()
+        ends[i].record(cur)
+        if flush is not None:
+            flush.zero_()
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    return {"ms_per_step": statistics.mean(ms), "median_ms": statistics.median(ms), "steps": steps}
 
 
 def run_gather_p1(torch, sel, spec, w, cu, cu_dev, hid_dev, pos_dev, slot_dev, out, peaks, launches=5):

@@ -486,3 +486,41 @@ def test_pass1_sweeps_again_after_a_huge_logit_jump(sel):
     got = out.scores.cpu().numpy()
     assert C.score_violations(got, ref, cu)["ok"]
     assert got[big] > 0.99
+
+
+def test_select_tokens_replays_from_a_cuda_graph(sel):
+    """The fused call captured once in a CUDA graph and replayed gives the eager call's results."""
+    spec = small_spec("graph", SMALL[1][1])
+    w = wl.generate(spec)
+    p = params_of(spec)
+    s = w.spec
+    q = _up(w.q_full_bits().view(np.int16)).view(torch.bfloat16)
+    k = _up(w.k_bits.view(np.int16)).view(torch.bfloat16)
+    hid = _up(w.hidden_bits().view(np.int16))
+    pos, slots, cu_dev = _up(w.positions()), _up(w.slots()), _up(w.cu_seqlens)
+    eager = sel.select_tokens(q, k, w.cu_seqlens, cu_dev, s.num_q_heads, s.num_kv_heads, s.head_dim, hid, pos, slots,
+                              params=p, kv_of_q=s.kv_of_q)
+    torch.cuda.synchronize()
+    eager = {f: getattr(eager, f).clone() for f in ("scores", "keep_bits", "kept_count", "cu_seqlens_out",
+                                                     "total_kept", "hidden_out", "pos_out", "slot_out")}
+    out = sel.alloc_outputs(w.cu_seqlens, s.block, hid, pos, slots)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        sel.select_tokens(q, k, w.cu_seqlens, cu_dev, s.num_q_heads, s.num_kv_heads, s.head_dim, hid, pos, slots,
+                          params=p, kv_of_q=s.kv_of_q, out=out)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=side):
+            sel.select_tokens(q, k, w.cu_seqlens, cu_dev, s.num_q_heads, s.num_kv_heads, s.head_dim, hid, pos,
+                              slots, params=p, kv_of_q=s.kv_of_q, out=out)
+    for f in eager:
+        getattr(out, f).zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert sel.status() == 0
+    total = int(eager["total_kept"].item())
+    for f in ("scores", "keep_bits", "kept_count", "cu_seqlens_out", "total_kept"):
+        assert torch.equal(getattr(out, f), eager[f]), f
+    for f in ("hidden_out", "pos_out", "slot_out"):
+        assert torch.equal(getattr(out, f)[:total], eager[f][:total]), f
