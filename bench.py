@@ -58,6 +58,10 @@ def parse_args():
     ap.add_argument("--top-p", type=float, default=None, help="override p (e.g. 1.0 keeps every token)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--stack", action="store_true",
+                    help="instead of the bench line: a synthetic stack of later layers on the kept tokens")
+    ap.add_argument("--stack-layers", type=int, default=48,
+                    help="layers in the synthetic stack (48: a multiple of both schedules' periods)")
     ap.add_argument("--no-graph", action="store_true", help="skip timing the step replayed from a CUDA graph")
     ap.add_argument("--no-gather-p1", action="store_true", help="skip the supplementary all-kept gather point")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -297,6 +301,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.stack:
+        return run_stack(args)
     import torch
     import torch.distributed as dist
 
@@ -493,6 +499,102 @@ def graph_replay(torch, step, stream, steps, flush):
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     return {"ms_per_step": statistics.mean(ms), "median_ms": statistics.median(ms), "steps": steps}
+
+
+def run_stack(args):
+    """Cumulative savings of token selection over a stack of later layers.
+
+    The layers are modelled by their token-proportional part only: a gated FFN
+    (LLaMA-3.1-8B sizes: hidden 4096, intermediate 14336; random bf16 weights
+    shared by all layers; residual add), run with cuBLAS through torch.  In a
+    hybrid schedule r:1, every (r+1)-th layer is a full-attention layer, where
+    the selection runs on the current tokens before its FFN and every later
+    layer sees only the kept ones.  The selection's inputs at every
+    full-attention layer are the workload's own tail queries and keys,
+    restricted to the surviving tokens (its planted structure stands in for a
+    trained model's attention, so the kept fraction is the synthetic
+    workload's, not a model's).  Attention and the linear-attention mixers are
+    not modelled.  The dense baseline runs the same layers on every token."""
+    import torch
+    from sparse_long_context_tail_gb300 import _binding as B
+    from sparse_long_context_tail_gb300.selector import TokenSelector
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    spec = wl.named_spec(args.workload)
+    w = wl.generate(spec)
+    cu = w.cu_seqlens
+    T, Hd, Hi = w.total_tokens, spec.hidden, 14336
+    params = B.make_params(spec.n_tail, spec.block, spec.sink_keep, spec.tail_keep, spec.top_p)
+    q_all = torch.zeros((T, spec.num_q_heads, spec.head_dim), dtype=torch.bfloat16, device=dev)
+    q_all[torch.from_numpy(w.tail_rows).to(dev)] = torch.from_numpy(w.q_tail_bits.view(np.int16)).view(
+        torch.bfloat16).to(dev)
+    k_all = torch.from_numpy(w.k_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    x0 = torch.from_numpy(w.hidden_bits().view(np.int16)).to(dev).view(torch.bfloat16)
+    g = torch.Generator(device=dev).manual_seed(7)
+    wg = (torch.randn((Hi, Hd), generator=g, device=dev) / math.sqrt(Hd)).to(torch.bfloat16)
+    wu = (torch.randn((Hi, Hd), generator=g, device=dev) / math.sqrt(Hd)).to(torch.bfloat16)
+    wd = (torch.randn((Hd, Hi), generator=g, device=dev) / math.sqrt(Hi)).to(torch.bfloat16)
+    sel = TokenSelector(0)
+    F = torch.nn.functional
+
+    def ffn(x):
+        return x + F.linear(F.silu(F.linear(x, wg)) * F.linear(x, wu), wd)
+
+    def run(full_every):
+        x, idx, cu_cur = x0, None, cu
+        tokens, sel_ms = [], 0.0
+        for layer in range(args.stack_layers):
+            if full_every and (layer + 1) % full_every == 0:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                q = q_all if idx is None else q_all.index_select(0, idx)
+                k = k_all if idx is None else k_all.index_select(0, idx)
+                out = sel.select_tokens(q, k, cu_cur, torch.from_numpy(cu_cur).to(dev), spec.num_q_heads,
+                                        spec.num_kv_heads, spec.head_dim, x.view(torch.int16), params=params,
+                                        kv_of_q=spec.kv_of_q)
+                e1.record()
+                kept = int(out.total_kept.item())
+                cu_cur = out.cu_seqlens_out.cpu().numpy().astype(np.int32)
+                ki = out.kept_index[:kept].long()
+                idx = ki if idx is None else idx.index_select(0, ki)
+                x = out.hidden_out[:kept].view(torch.bfloat16)
+                sel_ms += e0.elapsed_time(e1)
+            x = ffn(x)
+            tokens.append(int(x.shape[0]))
+        return tokens, sel_ms
+
+    def timed(full_every, reps=2):
+        run(full_every)                                   # warm-up (allocations, cuBLAS plans)
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            tokens, sel_ms = run(full_every)
+            torch.cuda.synchronize()
+            dt = (time.perf_counter() - t0) * 1e3
+            best = dt if best is None or dt < best else best
+        return best, tokens, sel_ms
+
+    dense_ms, _, _ = timed(0)
+    flop_layer = 2.0 * 3 * Hd * Hi
+    result = {"mode": "stack", "workload": spec.name, "layers": args.stack_layers,
+              "ffn": {"hidden": Hd, "intermediate": Hi, "gemm": "cuBLAS bf16 via torch"},
+              "dense_ms": dense_ms, "dense_ffn_tflops": flop_layer * T * args.stack_layers / dense_ms / 1e9,
+              "schedules": {}}
+    for name, every in (("3:1", 4), ("5:1", 6)):
+        ms, tokens, sel_ms = timed(every)
+        full = [i for i in range(args.stack_layers) if (i + 1) % every == 0]
+        result["schedules"][name] = {
+            "full_attention_layers": full, "ms": ms, "speedup_vs_dense": dense_ms / ms,
+            "saved_fraction": 1.0 - ms / dense_ms, "selection_ms": sel_ms,
+            "tokens_after_each_full_layer": [tokens[i] for i in full],
+            "token_layers_fraction": sum(tokens) / float(T * args.stack_layers)}
+    result["note"] = ("layers modelled by their gated FFN only (the token-proportional part); selection at each "
+                      "full-attention layer on the synthetic workload's own queries and keys; kept fractions are "
+                      "the synthetic workload's, not a trained model's")
+    print(json.dumps(result), flush=True)
+    sel.close()
+    return 0
 
 
 def run_gather_p1(torch, sel, spec, w, cu, cu_dev, hid_dev, pos_dev, slot_dev, out, peaks, launches=5):
