@@ -6,18 +6,19 @@
 // (positions, KV-cache slot addresses) follows the drop, and each drop records
 // the layer id and the number of kept tokens.
 //
-// Three launches: (1) popcount per chunk of 1024 keep-bit words; (2) per chunk,
-// a block scan of word popcounts gives every kept token its output row, written
-// to kept_index, plus the compacted cu_seqlens of the requests that start in the
-// chunk; (3) a persistent gather, one warp per output row, moving hidden rows
-// with 16-byte vector loads/stores, plus the history append.
+// Three launches: (1) popcount per chunk of 4096 keep-bit words (skipped when
+// the batch fits one chunk, up to 131072 tokens); (2) per chunk, a block scan of
+// word popcounts gives every kept token its output row, written to kept_index,
+// plus the compacted cu_seqlens of the requests that start in the chunk; (3) a
+// persistent gather, one warp per output row, moving hidden rows with 16-byte
+// vector loads/stores, plus the history append.
 #include "upf_internal.cuh"
 
 namespace upf {
 
 namespace {
 
-constexpr int kChunkThreads = 256;
+constexpr int kChunkThreads = 1024;
 
 // Keep-bit word w with any bits past token T cleared (defensive: a caller's
 // mask may carry stray bits there, which must not produce rows past T).
@@ -28,6 +29,7 @@ __device__ __forceinline__ uint32_t load_word(const CompactArgs& a, int w) {
   return x;
 }
 constexpr int kWordsPerThread = kCompactChunkWords / kChunkThreads;  // 4
+static_assert(kWordsPerThread * kChunkThreads == kCompactChunkWords, "a chunk is split evenly");
 
 __device__ __forceinline__ int block_sum(int v, int* s_tmp) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -60,6 +62,7 @@ __global__ void __launch_bounds__(kChunkThreads) compact_index_kernel(const Comp
   pdl_wait();
   __shared__ int s_tmp[kChunkThreads / 32];
   __shared__ int s_woff[kCompactChunkWords + 1];  // exclusive kept-token prefix per word of the chunk
+  __shared__ uint32_t s_word[kCompactChunkWords];
   __shared__ int s_warp[kChunkThreads / 32];
   const int c = blockIdx.x, tid = threadIdx.x;
   // Kept tokens in earlier chunks.
@@ -90,18 +93,19 @@ __global__ void __launch_bounds__(kChunkThreads) compact_index_kernel(const Comp
   int run = woff + incl - mine;
   for (int i = 0; i < kWordsPerThread; ++i) {
     s_woff[tid * kWordsPerThread + i] = run;
-    uint32_t bits = words[i];
-    const int wtok = (c * kCompactChunkWords + tid * kWordsPerThread + i) * 32;
-    int out = base + run;
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      bits &= bits - 1;
-      a.kept_index[out++] = wtok + b;
-    }
+    s_word[tid * kWordsPerThread + i] = words[i];
     run += pc[i];
   }
   if (tid == blockDim.x - 1) s_woff[kCompactChunkWords] = run;
   __syncthreads();
+  // Output rows: one word per warp at a time, lane b writing the row of bit
+  // b, so each warp's stores are consecutive.
+  for (int wl = warp; wl < kCompactChunkWords; wl += kChunkThreads / 32) {
+    const uint32_t word = s_word[wl];
+    if ((word >> lane) & 1u)
+      a.kept_index[base + s_woff[wl] + __popc(word & ((1u << lane) - 1u))] =
+          (c * kCompactChunkWords + wl) * 32 + lane;
+  }
   // Compacted cu_seqlens: boundary r lies in this chunk if its first token
   // does; the last chunk also takes every boundary at or past its start
   // (including cu[R] = T).

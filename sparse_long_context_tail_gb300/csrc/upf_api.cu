@@ -450,10 +450,16 @@ cudaError_t staged(upf_ctx* ctx, int stage, cudaStream_t s, F&& f) {
 
 enum Stage { kDescribe = 0, kPass1, kPass2, kFinalize, kSelect, kCompactCount, kCompactIndex, kCompactGather };
 
-// chained: the count kernel follows another kernel of the same call (PDL).
+// chained: the first compaction kernel follows another kernel of the same call
+// (PDL).  A batch of one chunk needs no chunk totals: its index kernel starts
+// from zero.
 upf_status launch_compact_all(upf_ctx* ctx, const upf::CompactArgs& ca, cudaStream_t s, bool chained) {
-  UPF_LAUNCH(staged(ctx, kCompactCount, s, [&] { return upf::launch_compact_count(ca, s, chained); }), "compact count");
-  UPF_LAUNCH(staged(ctx, kCompactIndex, s, [&] { return upf::launch_compact_index(ca, s, true); }), "compact index");
+  if (ca.nchunks > 1)
+    UPF_LAUNCH(staged(ctx, kCompactCount, s, [&] { return upf::launch_compact_count(ca, s, chained); }),
+               "compact count");
+  const bool index_chained = ca.nchunks > 1 || chained;
+  UPF_LAUNCH(staged(ctx, kCompactIndex, s, [&] { return upf::launch_compact_index(ca, s, index_chained); }),
+             "compact index");
   UPF_LAUNCH(staged(ctx, kCompactGather, s, [&] { return upf::launch_compact_gather(ca, s, true); }), "compact gather");
   return UPF_OK;
 }

@@ -25,7 +25,7 @@ namespace upf {
 
 constexpr int kMaxHeads = 256;         // H_q limit (the q-head list travels by value)
 constexpr int kMaxBlocksPerReq = 16384;  // select kernel sorts up to this many blocks in shared memory
-constexpr int kCompactChunkWords = 1024;  // keep-bit words per compaction chunk (32768 tokens)
+constexpr int kCompactChunkWords = 4096;  // keep-bit words per compaction chunk (131072 tokens)
 constexpr int kPlanSMs = 152;             // SM count the work split is planned for (GB300)
 // Partial rows the tensor-core passes write per (kv head, query chunk) and
 // per pass-1 item row (the epilogue warps that split a unit's columns merge

@@ -294,6 +294,43 @@ def test_compact_all_and_none(sel):
             assert torch.equal(hout, hid) and torch.equal(kidx.cpu(), torch.arange(T, dtype=torch.int32))
 
 
+
+def test_compact_spans_several_chunks(sel):
+    """Random keep bits over more tokens than one scan chunk holds (131072), with
+    request boundaries on, just before and just after the chunk edges and an
+    empty request: every output is bit-exact against the oracle."""
+    rng = np.random.default_rng(11)
+    T = 3 * 131072 + 4321
+    cu = np.array([0, 5, 131071, 131072, 131073, 131073, 262144, 262175, 300000, T], dtype=np.int32)
+    R = len(cu) - 1
+    mask = rng.random(T) < 0.3
+    mask[131000:131200] = True
+    mask[262100:262200] = False
+    cu_dev = _up(cu)
+    batch, keep = B.make_batch(cu_dev.data_ptr(), cu, 1, 1, 64)
+    nbytes = B.upf_workspace_bytes(batch, B.make_params())
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    bits = _up(C.pack_bits(mask).view(np.int32))
+    hid_np = rng.integers(-30000, 30000, size=(T, 8), dtype=np.int16)
+    pos_np = rng.integers(0, 1 << 40, size=T, dtype=np.int64)
+    hid, pos = _up(hid_np), _up(pos_np)
+    hout, pout = torch.empty_like(hid), torch.empty_like(pos)
+    kidx = torch.empty(T, dtype=torch.int32, device=DEV)
+    cuo = torch.empty(R + 1, dtype=torch.int32, device=DEV)
+    tot = torch.empty(1, dtype=torch.int32, device=DEV)
+    io = B.make_compact_io(16, hid.data_ptr(), hout.data_ptr(), pos.data_ptr(), pout.data_ptr(),
+                           kept_index=kidx.data_ptr(), cu_seqlens_out=cuo.data_ptr(), total_kept=tot.data_ptr())
+    B.upf_compact(sel.ctx, batch, bits.data_ptr(), io, ws.data_ptr(), nbytes, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert sel.status() == 0
+    comp = oracle.compact(mask, cu, hid_np, pos_np)
+    total = comp["total_kept"]
+    assert int(tot.item()) == total
+    np.testing.assert_array_equal(cuo.cpu().numpy(), comp["cu_seqlens_out"])
+    np.testing.assert_array_equal(kidx[:total].cpu().numpy(), comp["kept_index"])
+    np.testing.assert_array_equal(hout[:total].cpu().numpy(), comp["hidden_out"])
+    np.testing.assert_array_equal(pout[:total].cpu().numpy(), comp["positions_out"])
+
 def test_nonfinite_scores_are_reported(sel):
     cu = np.array([0, 640, 1000], dtype=np.int32)
     T = 1000
