@@ -2,6 +2,7 @@
 
 * ``_binding``: ctypes binding of the C ABI in ``include/upf.h`` (same names).
 * ``selector``: torch-tensor front end (``TokenSelector.select_tokens``).
+* ``tp``: heads sharded over tensor-parallel ranks, one score all-reduce.
 * ``workload``: seeded synthetic inputs (no method arithmetic).
 * ``build``: compiles ``libupf.so`` in-tree for sm_103a.
 
@@ -10,11 +11,11 @@ missing library raises.
 """
 import importlib
 
-__all__ = ["workload", "build", "_binding", "selector", "TokenSelector"]
+__all__ = ["workload", "build", "_binding", "selector", "tp", "TokenSelector"]
 
 
 def __getattr__(name):
-    if name in ("workload", "build", "_binding", "selector"):
+    if name in ("workload", "build", "_binding", "selector", "tp"):
         return importlib.import_module(f".{name}", __name__)
     if name == "TokenSelector":
         return importlib.import_module(".selector", __name__).TokenSelector

@@ -118,3 +118,54 @@ class TokenSelector:
                             io, ws.data_ptr(), ws.numel(), stream)
         del keep
         return out
+
+    def score(self, q: torch.Tensor, k: torch.Tensor, cu_seqlens_host: np.ndarray, cu_seqlens_dev: torch.Tensor,
+              num_q_heads: int, num_kv_heads: int, head_dim: int, params: Optional[B.UpfParams] = None,
+              kv_of_q: Optional[Sequence[int]] = None, scores: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """Token importances alone (``upf_score``): float32 [T] on the selector's GPU.
+
+        q and k may be views of a wider tensor (a head range of every row): the
+        row strides are passed through."""
+        params = params or B.make_params()
+        batch, keep = B.make_batch(cu_seqlens_dev.data_ptr(), cu_seqlens_host, num_q_heads, num_kv_heads,
+                                   head_dim, kv_of_q)
+        nbytes = B.upf_workspace_bytes(batch, params)
+        ws = self.workspace(nbytes)
+        T = int(cu_seqlens_host[-1])
+        if scores is None:
+            scores = torch.empty(T, dtype=torch.float32, device=self.device)
+        stream = torch.cuda.current_stream(self.device).cuda_stream
+        B.upf_score(self.ctx, batch, params, q.data_ptr(), q.stride(0), k.data_ptr(), k.stride(0), scores.data_ptr(),
+                    ws.data_ptr(), ws.numel(), stream)
+        del keep
+        return scores
+
+    def select_compact(self, scores: torch.Tensor, cu_seqlens_host: np.ndarray, cu_seqlens_dev: torch.Tensor,
+                       hidden: Optional[torch.Tensor] = None, positions: Optional[torch.Tensor] = None,
+                       slots: Optional[torch.Tensor] = None, layer_id: int = 0,
+                       history: Optional[torch.Tensor] = None, history_len: Optional[torch.Tensor] = None,
+                       params: Optional[B.UpfParams] = None, out: Optional[SelectOutputs] = None) -> SelectOutputs:
+        """``upf_select`` then ``upf_compact`` on given token scores (e.g. scores
+        summed over tensor-parallel ranks); ``out.scores`` is set to ``scores``."""
+        params = params or B.make_params()
+        # selection and compaction read only the request layout from the batch
+        batch, keep = B.make_batch(cu_seqlens_dev.data_ptr(), cu_seqlens_host, 1, 1, 64)
+        nbytes = B.upf_workspace_bytes(batch, params)
+        ws = self.workspace(nbytes)
+        if out is None:
+            out = self.alloc_outputs(cu_seqlens_host, params.block, hidden, positions, slots)
+        out.scores = scores
+        stream = torch.cuda.current_stream(self.device).cuda_stream
+        B.upf_select(self.ctx, batch, params, scores.data_ptr(), _ptr(out.block_scores), _ptr(out.keep_bits),
+                     _ptr(out.kept_count), ws.data_ptr(), ws.numel(), stream)
+        io = B.make_compact_io(
+            row_bytes=0 if hidden is None else hidden.stride(0) * hidden.element_size(),
+            hidden_in=_ptr(hidden), hidden_out=_ptr(out.hidden_out), pos_in=_ptr(positions),
+            pos_out=_ptr(out.pos_out), slot_in=_ptr(slots), slot_out=_ptr(out.slot_out),
+            kept_index=_ptr(out.kept_index), cu_seqlens_out=_ptr(out.cu_seqlens_out),
+            total_kept=_ptr(out.total_kept), layer_id=layer_id,
+            history_cap=0 if history is None else history.shape[1], history=_ptr(history),
+            history_len=_ptr(history_len))
+        B.upf_compact(self.ctx, batch, out.keep_bits.data_ptr(), io, ws.data_ptr(), ws.numel(), stream)
+        del keep
+        return out

@@ -1,0 +1,130 @@
+"""Tensor-parallel score exchange on CPU ranks (gloo, world size 2).
+
+Each rank scores only its own heads (here with the oracle, on the CPU), the
+ranks average their local scores with one all-reduce, and the result must be
+the all-heads score on every rank, bit-identical across ranks, with the same
+selection.  A rank that dies before the exchange makes the other rank's
+exchange fail with an error instead of hanging.
+"""
+import datetime
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import oracle
+from sparse_long_context_tail_gb300 import tp
+from sparse_long_context_tail_gb300 import workload as wl
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _spec():
+    return wl.WorkloadSpec("tp-cpu", [700, 1300], 8, 4, 64, 64, n_tail=32, block=32, planted=[2, 3],
+                           strength_range=(1.0, 4.0), seed=91)
+
+
+def _local_scores(w, rank, world):
+    s = w.spec
+    qs, ks = tp.shard_heads(s.num_q_heads, s.num_kv_heads, rank, world)
+    return oracle.token_scores(np.ascontiguousarray(w.k_bits[:, ks]), np.ascontiguousarray(w.q_tail_bits[:, qs]),
+                               w.cu_seqlens, qs.stop - qs.start, ks.stop - ks.start, s.head_dim, s.n_tail)
+
+
+def _exchange_worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=60))
+    try:
+        w = wl.generate(_spec())
+        local = torch.from_numpy(_local_scores(w, rank, world))
+        tp.allreduce_scores(local)
+        out[rank] = local.numpy().tobytes()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_shard_heads_covers_every_group_once():
+    seen_q, seen_kv = [], []
+    for r in range(4):
+        qs, ks = tp.shard_heads(32, 8, r, 4)
+        assert (qs.stop - qs.start, ks.stop - ks.start) == (8, 2)
+        # every q head of the shard reads a kv head of the same shard (contiguous GQA groups)
+        assert all(ks.start <= h // 4 < ks.stop for h in range(qs.start, qs.stop))
+        seen_q += list(range(qs.start, qs.stop))
+        seen_kv += list(range(ks.start, ks.stop))
+    assert seen_q == list(range(32)) and seen_kv == list(range(8))
+    with pytest.raises(ValueError):
+        tp.shard_heads(32, 8, 0, 3)
+    with pytest.raises(ValueError):
+        tp.shard_heads(32, 8, 2, 2)
+
+
+def test_mean_of_partials_is_the_all_heads_score():
+    w = wl.generate(_spec())
+    s = w.spec
+    full = oracle.token_scores(w.k_bits, w.q_tail_bits, w.cu_seqlens, s.num_q_heads, s.num_kv_heads, s.head_dim,
+                               s.n_tail)
+    for world in (2, 4):
+        got = tp.mean_of_partials([torch.from_numpy(_local_scores(w, r, world)) for r in range(world)]).numpy()
+        np.testing.assert_allclose(got, full, rtol=1e-12, atol=1e-300)
+
+
+def test_two_ranks_exchange_scores():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_exchange_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=180)
+        assert p.exitcode == 0
+    assert out[0] == out[1]                          # every rank holds the same bits
+    w = wl.generate(_spec())
+    s = w.spec
+    got = np.frombuffer(out[0], dtype=np.float64)
+    full = oracle.token_scores(w.k_bits, w.q_tail_bits, w.cu_seqlens, s.num_q_heads, s.num_kv_heads, s.head_dim,
+                               s.n_tail)
+    np.testing.assert_allclose(got, full, rtol=1e-12, atol=1e-300)
+    a = oracle.select(got, w.cu_seqlens, s.block, s.top_p, s.sink_keep, s.tail_keep)
+    b = oracle.select(full, w.cu_seqlens, s.block, s.top_p, s.sink_keep, s.tail_keep)
+    np.testing.assert_array_equal(a["mask"], b["mask"])
+
+
+def _dead_peer_worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=10))
+    if rank == 1:
+        os._exit(0)                                  # dies before the exchange
+    try:
+        tp.allreduce_scores(torch.ones(64, dtype=torch.float64))
+        out[rank] = "returned"
+    except Exception as e:                           # noqa: BLE001 - any error is the expected outcome
+        out[rank] = "raised: " + type(e).__name__
+    os._exit(0)
+
+
+def test_dead_rank_fails_the_exchange_instead_of_hanging():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_dead_peer_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    alive = [p for p in procs if p.is_alive()]
+    for p in alive:
+        p.kill()
+    assert not alive, "a rank hung in the exchange"
+    assert out.get(0, "").startswith("raised"), out.get(0)
