@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(256) block_means_kernel(const SelectArgs a) {
       float v;
       if (a.P > 0) {
         v = 0.f;
+        // partials in a fixed order; the unrolled loads are in flight together
+#pragma unroll 8
         for (int c = 0; c < a.P; ++c) v += a.part[(int64_t)c * a.T + tok0 + t];
         v *= inv;
         if (a.scores_out) a.scores_out[tok0 + t] = v;
@@ -274,7 +276,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
   int cnt = 0;
   for (int i = tid; i < nb; i += blockDim.x)
     if (keep[i]) cnt += min(L, (i + 1) * a.G) - i * a.G;
-  atomicAdd(&s_cnt, cnt);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if (lane == 0 && cnt) atomicAdd(&s_cnt, cnt);
   // Keep bits of packed tokens [tok0, tok0 + L): interior words by plain
   // stores, the two words shared with neighbour requests by atomicOr.
   const int w0 = tok0 >> 5, w1 = (tok0 + L - 1) >> 5;
