@@ -100,6 +100,58 @@ def test_two_ranks_exchange_scores():
     np.testing.assert_array_equal(a["mask"], b["mask"])
 
 
+class _FakeSelector:
+    """Stands in for TokenSelector on the CPU: records what tp_select_tokens passes."""
+
+    def __init__(self, local_scores):
+        self.local_scores = local_scores
+        self.calls = []
+
+    def score(self, q, k, cu_host, cu_dev, hq, hkv, d, params=None):
+        self.calls.append(("score", hq, hkv, d, tuple(q.shape), tuple(k.shape)))
+        return self.local_scores.clone()
+
+    def select_compact(self, scores, cu_host, cu_dev, hidden, positions, slots, layer_id, history, history_len,
+                       params, out):
+        self.calls.append(("select_compact", layer_id))
+        return scores
+
+
+def _glue_worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=60))
+    try:
+        T, hq, hkv, d = 50, 8, 4, 64
+        qs, ks = tp.shard_heads(hq, hkv, rank, world)
+        q = torch.zeros(T, hq, d)[:, qs]
+        k = torch.zeros(T, hkv, d)[:, ks]
+        sel = _FakeSelector(torch.arange(T, dtype=torch.float32) * (rank + 1))
+        got = tp.tp_select_tokens(sel, q, k, np.array([0, T]), torch.tensor([0, T]), qs.stop - qs.start,
+                                  ks.stop - ks.start, d, layer_id=7)
+        out[rank] = (got.numpy().tobytes(), sel.calls)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_tp_select_tokens_scores_locally_then_selects_on_the_mean():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_glue_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    (b0, c0), (b1, c1) = out[0], out[1]
+    assert b0 == b1
+    want = (np.arange(50, dtype=np.float32) * 1.5)          # mean of 1x and 2x the local scores
+    np.testing.assert_array_equal(np.frombuffer(b0, dtype=np.float32), want)
+    for calls in (c0, c1):
+        assert calls == [("score", 4, 2, 64, (50, 4, 64), (50, 2, 64)), ("select_compact", 7)]
+
+
 def _dead_peer_worker(rank, world, port, out):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=10))
