@@ -501,6 +501,12 @@ def graph_replay(torch, step, stream, steps, flush):
     return {"ms_per_step": statistics.mean(ms), "median_ms": statistics.median(ms), "steps": steps}
 
 
+def full_attention_layers(layers, every):
+    """Indices of the full-attention layers of an (every-1):1 hybrid stack: the
+    last layer of every group of `every`."""
+    return [i for i in range(layers) if (i + 1) % every == 0]
+
+
 def run_stack(args):
     """Cumulative savings of token selection over a stack of later layers.
 
@@ -543,8 +549,9 @@ def run_stack(args):
     def run(full_every):
         x, idx, cu_cur = x0, None, cu
         tokens, sel_ms = [], 0.0
+        full = set(full_attention_layers(args.stack_layers, full_every)) if full_every else set()
         for layer in range(args.stack_layers):
-            if full_every and (layer + 1) % full_every == 0:
+            if layer in full:
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
                 q = q_all if idx is None else q_all.index_select(0, idx)
@@ -583,7 +590,7 @@ def run_stack(args):
               "schedules": {}}
     for name, every in (("3:1", 4), ("5:1", 6)):
         ms, tokens, sel_ms = timed(every)
-        full = [i for i in range(args.stack_layers) if (i + 1) % every == 0]
+        full = full_attention_layers(args.stack_layers, every)
         result["schedules"][name] = {
             "full_attention_layers": full, "ms": ms, "speedup_vs_dense": dense_ms / ms,
             "saved_fraction": 1.0 - ms / dense_ms, "selection_ms": sel_ms,
