@@ -560,7 +560,11 @@ __device__ __forceinline__ void pass1_epilogue(const ScoreArgs& a, const Smem& s
   float m0, m1, m2, m3, z0, z1, z2, z3;
   const uint32_t tbase = tmem + (uint32_t(qd * 32) << 16) + uint32_t(cb * span);
   bool ok = true;
-  int uidx = 0;
+  // TMEM slot of the next unit and its phase parity, advanced without a
+  // division (the slot count is 2 or 4, known only at run time); the sequence
+  // continues into a second sweep as the MMA's does.
+  int slot_next = 0;
+  uint32_t slot_par = 0;
   auto sweep = [&](auto checked_flag) -> bool {   // returns: some sum not finite (fast path only)
     constexpr bool kChecked = decltype(checked_flag)::value;
     m0 = m1 = m2 = m3 = -INFINITY;
@@ -570,12 +574,16 @@ __device__ __forceinline__ void pass1_epilogue(const ScoreArgs& a, const Smem& s
       const int kt = k0 + i * geo.tile_keys;   // request-relative first key of the tile
       const bool masked = kt + geo.tile_keys - 1 > it.L - a.n;
 #pragma unroll
-      for (int h = 0; h < 4; ++h, ++uidx) {
+      for (int h = 0; h < 4; ++h) {
         if (h >= MT) break;
-        const int slot = uidx % geo.nslots;
-        if (!wait_slot_fast(a, sm, slot, (uidx / geo.nslots) & 1)) {
+        const int slot = slot_next;
+        if (!wait_slot_fast(a, sm, slot, slot_par)) {
           ok = false;
           break;
+        }
+        if (++slot_next == geo.nslots) {
+          slot_next = 0;
+          slot_par ^= 1u;
         }
         const int lh = h == 0 ? l0 : h == 1 ? l1 : h == 2 ? l2 : l3;
         float mh = h == 0 ? m0 : h == 1 ? m1 : h == 2 ? m2 : m3;
