@@ -176,6 +176,10 @@ size_t upf_workspace_bytes(const upf_batch* batch, const upf_params* params);
  *    k_row_stride >= H_kv*d, a multiple of 8.  q and k 16-byte aligned.
  * scores: device float32 [T].
  * ws / ws_bytes: workspace of at least upf_workspace_bytes() bytes.
+ * q and k may point at a range of heads inside wider rows (the row strides
+ * stay those of the full rows): a tensor-parallel rank scores its own heads
+ * this way, normalised over the heads it was given (section 三, multi-GPU:
+ * the ranks' scores are then summed before the decision).
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 upf_status upf_score(upf_ctx* ctx, const upf_batch* batch, const upf_params* params,
                      const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
