@@ -64,7 +64,13 @@ def tp_select_tokens(sel: TokenSelector, q_local: torch.Tensor, k_local: torch.T
     q_local / k_local: this rank's head slices ([T, H_q/P, d] / [T, H_kv/P, d],
     views with the full row strides are fine).  Scores the local heads, averages
     the scores over the ranks of `group` (one all-reduce), then selects and
-    compacts exactly as the single-GPU call does."""
+    compacts exactly as the single-GPU call does.  Shapes are checked before
+    any collective, so a rank with the wrong slice fails alone and at once."""
+    for name, t, heads in (("q_local", q_local, local_q_heads), ("k_local", k_local, local_kv_heads)):
+        if t.dim() != 3 or t.shape[1] != heads or t.shape[2] != head_dim:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected [T, {heads}, {head_dim}]")
+    if q_local.shape[0] != k_local.shape[0] or q_local.shape[0] != int(cu_seqlens_host[-1]):
+        raise ValueError("q_local, k_local and cu_seqlens disagree on the token count")
     scores = sel.score(q_local, k_local, cu_seqlens_host, cu_seqlens_dev, local_q_heads, local_kv_heads,
                        head_dim, params=params)
     allreduce_scores(scores, group)

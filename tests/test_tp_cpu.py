@@ -152,6 +152,19 @@ def test_tp_select_tokens_scores_locally_then_selects_on_the_mean():
         assert calls == [("score", 4, 2, 64, (50, 4, 64), (50, 2, 64)), ("select_compact", 7)]
 
 
+def test_tp_select_tokens_rejects_a_wrong_head_slice_before_any_exchange():
+    sel = _FakeSelector(torch.zeros(50))
+    q, k = torch.zeros(50, 4, 64), torch.zeros(50, 2, 64)
+    cu = np.array([0, 50])
+    with pytest.raises(ValueError, match="q_local"):
+        tp.tp_select_tokens(sel, q, k, cu, torch.tensor(cu), 8, 2, 64)
+    with pytest.raises(ValueError, match="k_local"):
+        tp.tp_select_tokens(sel, q, k, cu, torch.tensor(cu), 4, 4, 64)
+    with pytest.raises(ValueError, match="token count"):
+        tp.tp_select_tokens(sel, q, k, np.array([0, 49]), torch.tensor([0, 49]), 4, 2, 64)
+    assert sel.calls == []                           # nothing was scored, no collective was entered
+
+
 def _dead_peer_worker(rank, world, port, out):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=10))
