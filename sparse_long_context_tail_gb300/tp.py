@@ -65,7 +65,8 @@ def tp_select_tokens(sel: TokenSelector, q_local: torch.Tensor, k_local: torch.T
     views with the full row strides are fine).  Scores the local heads, averages
     the scores over the ranks of `group` (one all-reduce), then selects and
     compacts exactly as the single-GPU call does.  Shapes are checked before
-    any collective, so a rank with the wrong slice fails alone and at once."""
+    the exchange: a rank given the wrong slice raises without entering it, and
+    the other ranks' exchange then fails on the process group's timeout."""
     for name, t, heads in (("q_local", q_local, local_q_heads), ("k_local", k_local, local_kv_heads)):
         if t.dim() != 3 or t.shape[1] != heads or t.shape[2] != head_dim:
             raise ValueError(f"{name} has shape {tuple(t.shape)}, expected [T, {heads}, {head_dim}]")
