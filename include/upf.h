@@ -264,7 +264,12 @@ upf_status upf_history_kv_len(upf_ctx* ctx, const upf_batch* batch, const int32_
  * (and 16384 per request); larger batches return UPF_ERR_UNSUPPORTED.
  * status_dev: device int32 [1] (nullable) that receives device-detected
  * errors (first error wins; the caller clears it); when NULL such errors go to
- * a status word inside the array and are not reported.
+ * a status word inside the array and are not reported.  Pass status_dev:
+ * without it a failed call cannot be told from a good one.  What the outputs
+ * then hold: a request with a NaN, infinite or negative block score keeps all
+ * its tokens (as in upf_select); if cu_seqlens_dev disagrees with
+ * cu_seqlens_host, the device descriptor is zeroed, so every keep bit is 0
+ * and every kept_count is 0 -- the sink and tail tokens included.
  * The array is shared by every call and keeps the last call's contents; each
  * call rewrites what it reads.  Calls whose GPU work overlaps (different
  * streams or host threads) race on it: serialise them.  The first call on a

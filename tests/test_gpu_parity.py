@@ -405,9 +405,11 @@ def test_repeat_calls_are_deterministic(sel):
 
 # ----------------------------------------------- the benchmark workloads ----
 
-FULL = ["small-L4096", "llama8b-L32768", "llama8b-L131072", "llama8b-batch16",
-        "qwen3next-G64-n128", "gemma3-G64-n128", "qwen3next-G32-n512", "gemma3-G128-n32",
-        "qwen3next-G128-n32", "gemma3-G32-n512"]
+# Every benchmark workload at full size: the four LLaMA-shaped / small ones and
+# all eighteen Qwen3-Next / Gemma-3 sweep points (G in {32, 64, 128} x n in
+# {32, 128, 512} for each shape).
+FULL = ["small-L4096", "llama8b-L32768", "llama8b-L131072", "llama8b-batch16"] + list(wl.SWEEP_NAMES)
+assert len(FULL) == 22
 
 
 @pytest.mark.parametrize("name", FULL)

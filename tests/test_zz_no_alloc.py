@@ -11,6 +11,8 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
+from oracle import compare as C
 from sparse_long_context_tail_gb300 import _binding as B
 
 pytestmark = pytest.mark.gpu
@@ -74,6 +76,19 @@ def run_both(lengths, seed, block, top_p, pass_block_scores):
     if pass_block_scores:
         # same kernels on the same scores: block means agree within the score tolerance (in fact exactly)
         assert torch.allclose(bs_a, bs_b, rtol=1e-3, atol=1e-6 / max(lengths))
+    # and against the float64 oracle on the same float32 scores: the mask is the
+    # oracle's outside boundary blocks and exactly the top-p rule on the block
+    # means the call produced; the counts follow the mask
+    scores_np = scores.cpu().numpy().astype(np.float64)
+    ref = oracle.select(scores_np, cu, block, params.top_p, params.sink_keep, params.tail_keep)
+    mask = C.unpack_bits(bits_b.cpu().numpy(), T)
+    assert C.mask_mismatches(mask, ref, cu, block, params.top_p, params.sink_keep, params.tail_keep) == []
+    own_bs = (bs_b if pass_block_scores else bs_a).cpu().numpy()[:nb]
+    ref_bs = np.concatenate(ref["block_scores"])
+    assert np.all(np.abs(own_bs - ref_bs) <= 1e-3 * np.abs(ref_bs) + 1e-6 / max(lengths))
+    assert C.self_consistency_mismatches(mask, own_bs, cu, block, params.top_p, params.sink_keep,
+                                         params.tail_keep) == []
+    assert cnt_b.cpu().numpy().tolist() == [int(mask[cu[r]:cu[r + 1]].sum()) for r in range(R)]
     return int(cnt_b.sum().item())
 
 
