@@ -185,6 +185,21 @@ upf_status upf_score(upf_ctx* ctx, const upf_batch* batch, const upf_params* par
                      const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
                      float* scores, void* ws, size_t ws_bytes, void* stream);
 
+/* upf_score for one tensor-parallel rank (section 三, multi-GPU: every GPU
+ * scores the heads it holds and the per-GPU scores are summed before the
+ * keep decision).  `batch` describes this rank's heads only (num_q_heads and
+ * num_kv_heads of the slice, q and k pointing at the slice inside wider rows
+ * as for upf_score); the scores are normalised by num_q_heads_total, the
+ * q-head count over all ranks:
+ *   s_k = 1/(num_q_heads_total * n_eff) * sum_{h of this rank} sum_j softmax_j(k),
+ * so the element-wise sum of the ranks' scores is upf_score's result over
+ * all heads (a plain sum all-reduce, no rescaling).  With num_q_heads_total =
+ * num_q_heads it is upf_score.  Errors: as upf_score; INVALID_ARG if
+ * num_q_heads_total < num_q_heads. */
+upf_status upf_score_shard(upf_ctx* ctx, const upf_batch* batch, const upf_params* params,
+                           int32_t num_q_heads_total, const void* q, int64_t q_row_stride, const void* k,
+                           int64_t k_row_stride, float* scores, void* ws, size_t ws_bytes, void* stream);
+
 /* Block pooling, top-p selection, exemption and the binary keep mask (section
  * 二, second step and exemption paragraph; section 三, binary mask).  Per
  * request: block means b_i over blocks [iG, min((i+1)G, L)); rank blocks by
@@ -282,6 +297,18 @@ upf_status upf_history_kv_len(upf_ctx* ctx, const upf_batch* batch, const int32_
 upf_status upf_select_noalloc(const upf_batch* batch, const upf_params* params, const float* scores,
                               float* block_scores, uint32_t* keep_bits, int32_t* kept_count,
                               int32_t* status_dev, void* stream);
+
+/* Failure detection (not a step of the article's method).  Every wait
+ * inside the tensor-core scoring kernels is bounded; when one expires the
+ * kernel records UPF_ERR_TIMEOUT in the status word, stops issuing work,
+ * waits for its outstanding copies and MMAs, frees its tensor memory and
+ * returns, so the context stays usable.  This sets the limit of the pipeline
+ * waits (a role waiting for another role's data), in SM clock cycles, for
+ * later calls on `ctx`; 0 restores the default (4e9 cycles, about 2 s).  The
+ * waits that wind a kernel down always keep the default.  A very small limit
+ * makes a pipeline wait expire on purpose: that is how the timeout path is
+ * tested.  Errors: INVALID_ARG (ctx NULL, cycles < 0). */
+upf_status upf_set_wait_limit(upf_ctx* ctx, int64_t cycles);
 
 /* Tracing (per-stage device timing).  Stages, in launch order:
  * 0 describe (batch descriptor), 1 score pass 1, 2 score pass 2, 3 finalize /

@@ -58,6 +58,9 @@ _SIGNATURES = {
     "upf_workspace_bytes": ([POINTER(UpfBatch), POINTER(UpfParams)], c_size_t),
     "upf_score": ([c_void_p, POINTER(UpfBatch), POINTER(UpfParams), c_void_p, c_int64, c_void_p, c_int64,
                    c_void_p, c_void_p, c_size_t, c_void_p], c_int),
+    "upf_score_shard": ([c_void_p, POINTER(UpfBatch), POINTER(UpfParams), c_int32, c_void_p, c_int64, c_void_p,
+                         c_int64, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
+    "upf_set_wait_limit": ([c_void_p, c_int64], c_int),
     "upf_select": ([c_void_p, POINTER(UpfBatch), POINTER(UpfParams), c_void_p, c_void_p, c_void_p, c_void_p,
                     c_void_p, c_size_t, c_void_p], c_int),
     "upf_compact": ([c_void_p, POINTER(UpfBatch), c_void_p, POINTER(UpfCompactIO), c_void_p, c_size_t, c_void_p],
@@ -173,6 +176,16 @@ def upf_workspace_bytes(batch: UpfBatch, params: UpfParams) -> int:
 def upf_score(ctx, batch, params, q, q_row_stride, k, k_row_stride, scores, ws, ws_bytes, stream=0):
     _check(load().upf_score(ctx, ctypes.byref(batch), ctypes.byref(params), q, q_row_stride, k, k_row_stride,
                             scores, ws, ws_bytes, stream or None))
+
+
+def upf_score_shard(ctx, batch, params, num_q_heads_total, q, q_row_stride, k, k_row_stride, scores, ws, ws_bytes,
+                    stream=0):
+    _check(load().upf_score_shard(ctx, ctypes.byref(batch), ctypes.byref(params), num_q_heads_total, q, q_row_stride,
+                                  k, k_row_stride, scores, ws, ws_bytes, stream or None))
+
+
+def upf_set_wait_limit(ctx: int, cycles: int) -> None:
+    _check(load().upf_set_wait_limit(ctx, cycles))
 
 
 def upf_select(ctx, batch, params, scores, block_scores, keep_bits, kept_count, ws, ws_bytes, stream=0):

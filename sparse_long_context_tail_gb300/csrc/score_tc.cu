@@ -31,8 +31,10 @@
 // one tcgen05.commit cover a stage: per-slice commits were measured to stall
 // the tensor pipe.
 // Every wait is bounded; on a timeout the kernel records UPF_ERR_TIMEOUT, the
-// roles wind down, outstanding copies and MMAs are waited for (bounded), TMEM
-// is freed and the kernel returns.
+// roles wind down (the MMA issuer stops at the next tile once any role gave
+// up), outstanding copies and MMAs are waited for with the full limit, TMEM
+// is freed and the kernel returns.  The pipeline waits' limit is a run-time
+// argument (upf_set_wait_limit), so a test can make one expire.
 #include <cuda.h>
 
 #include <climits>
@@ -59,7 +61,9 @@ constexpr int kMaxSlots = 4;
 constexpr int kRedTiles = 8;
 constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxSlots + 3;   // + qfull, fin, decide                   // pass 2: tiles of per-key sums in flight
 constexpr int kSmemLimit = 232448;             // opt-in dynamic shared memory per CTA
-constexpr long long kWaitLimit = 4000000000LL; // clock cycles (about 2 s)
+// Waits that wind a kernel down (outstanding copies and MMAs before TMEM is
+// freed) always get the full limit; pipeline waits use ScoreArgs::wait_limit.
+constexpr long long kWaitLimit = kDefaultWaitCycles;
 constexpr uint32_t kIdleNs = 4000;              // longest suspension of a waiting role per poll
 
 __host__ __device__ constexpr int imin(int a, int b) { return a < b ? a : b; }
@@ -323,7 +327,7 @@ __device__ __forceinline__ void release_slot(const Smem& sm, int slot, int lane)
 // false (and the abort flag set) on a timeout or another role's abort.
 __device__ __forceinline__ bool wait_slot(const ScoreArgs& a, const Smem& sm, int slot, uint32_t parity) {
   if (aborted(sm)) return false;
-  if (!mbar_wait_idle(bar_tfull(sm, slot), parity, kWaitLimit, kIdleNs)) {
+  if (!mbar_wait_idle(bar_tfull(sm, slot), parity, a.wait_limit, kIdleNs)) {
     abort_with_timeout(a, sm);
     return false;
   }
@@ -368,7 +372,7 @@ __device__ int produce(const ScoreArgs& a, const CUtensorMap* tq_map, const CUte
   uint32_t ph = 0;
   for (int round = 0; round < (may_repeat ? 2 : 1); ++round) {
     if (round == 1) {   // pass 1: the tiles again only if the epilogue asks for it
-      if (!mbar_wait_idle(bar_decide(sm), 0, kWaitLimit, kIdleNs)) {
+      if (!mbar_wait_idle(bar_decide(sm), 0, a.wait_limit, kIdleNs)) {
         abort_with_timeout(a, sm);
         break;
       }
@@ -377,7 +381,7 @@ __device__ int produce(const ScoreArgs& a, const CUtensorMap* tq_map, const CUte
     int part = 0, key = it.tok0 + k0;
     for (int n = 0; n < total; ++n, ++q) {
       if (aborted(sm)) return q;
-      if (!mbar_wait_idle(bar_empty(sm, st), ph ^ 1u, kWaitLimit, kIdleNs)) {
+      if (!mbar_wait_idle(bar_empty(sm, st), ph ^ 1u, a.wait_limit, kIdleNs)) {
         abort_with_timeout(a, sm);
         return q;
       }
@@ -424,29 +428,34 @@ __device__ void issue_mma(const ScoreArgs& a, const Smem& sm, const Geo& geo, in
   const uint32_t ring0 = smem_u32(sm.ring), q0 = smem_u32(sm.q);
   const uint32_t q_slice = uint32_t(a.QC) * 128u;
   const uint32_t q_unit = uint32_t(keys_as_m ? geo.unit_cols : 128) * 128u;
-  bool ok = mbar_wait_idle(bar_qfull(sm), 0, kWaitLimit, kIdleNs);
+  bool ok = mbar_wait_idle(bar_qfull(sm), 0, a.wait_limit, kIdleNs);
   int st = 0;            // ring stage of the next tile's first part
   uint32_t ph = 0;       // its phase parity
   int slot = 0;          // TMEM slot of the next unit
   uint32_t sph = 0;      // its phase parity
   for (int round = 0; ok && round < (may_repeat ? 2 : 1); ++round) {
   if (round == 1) {        // pass 1: the tiles again only if the epilogue asks for it
-    ok = mbar_wait_idle(bar_decide(sm), 0, kWaitLimit, kIdleNs);
+    ok = mbar_wait_idle(bar_decide(sm), 0, a.wait_limit, kIdleNs);
     if (!ok || *reinterpret_cast<volatile int*>(sm.redo) == 0) break;
   }
   for (int i = 0; ok && i < ntiles; ++i) {
     // A tile takes spt <= 2 consecutive ring stages; slice s lives in stage
     // part s / sps at offset (s % sps) slices, sps in {1, 2}.
+    // Another role gave up (a timeout): issue nothing more.
+    if (aborted(sm)) {
+      ok = false;
+      break;
+    }
     const int st0 = st, st1 = st + 1 == geo.NS ? 0 : st + 1;
-    ok = mbar_wait_idle(bar_full(sm, st0), ph, kWaitLimit, kIdleNs);
-    if (ok && geo.spt == 2) ok = mbar_wait_idle(bar_full(sm, st1), st1 == 0 ? ph ^ 1u : ph, kWaitLimit, kIdleNs);
+    ok = mbar_wait_idle(bar_full(sm, st0), ph, a.wait_limit, kIdleNs);
+    if (ok && geo.spt == 2) ok = mbar_wait_idle(bar_full(sm, st1), st1 == 0 ? ph ^ 1u : ph, a.wait_limit, kIdleNs);
     if (geo.spt == 2) { st = st1 + 1 == geo.NS ? 0 : st1 + 1; ph = (st1 == 0 || st == 0) ? ph ^ 1u : ph; }
     else { st = st1; ph = st1 == 0 ? ph ^ 1u : ph; }
     const uint32_t k0a = ring0 + uint32_t(st0 * geo.stage_bytes), k1a = ring0 + uint32_t(st1 * geo.stage_bytes);
     if (!ok) break;
     tc_fence_after();
     for (int u = 0; u < units; ++u) {
-      ok = mbar_wait_idle(bar_tempty(sm, slot), sph ^ 1u, kWaitLimit, kIdleNs);
+      ok = mbar_wait_idle(bar_tempty(sm, slot), sph ^ 1u, a.wait_limit, kIdleNs);
       if (!ok) break;
       tc_fence_after();
       const uint32_t dt = tmem + uint32_t(slot * geo.slot_cols);
@@ -472,9 +481,12 @@ __device__ void issue_mma(const ScoreArgs& a, const Smem& sm, const Geo& geo, in
   }
   }
   if (!ok) abort_with_timeout(a, sm);
-  // Every MMA this warp issued must be done before TMEM can be freed.
+  // Every MMA this warp issued must be done before TMEM can be freed: this
+  // wait keeps the full limit whatever the pipeline limit is.  If even it
+  // expires, the error is recorded and TMEM is still freed (a CTA that left
+  // its columns allocated would stall the next CTA's allocation on this SM).
   if (leader) mma_commit(bar_fin(sm));
-  mbar_wait_idle(bar_fin(sm), 0, kWaitLimit, kIdleNs);
+  if (!mbar_wait_idle(bar_fin(sm), 0, kWaitLimit, kIdleNs)) abort_with_timeout(a, sm);
 }
 
 // Common prologue of both passes: barriers, padding, TMEM; returns the TMEM base.

@@ -18,6 +18,7 @@ struct upf_ctx {
   int device;
   int num_sms;
   int32_t* status_dev;  // [64] device words; [0] = status
+  long long wait_limit = 0;  // pipeline waits of the scoring kernels, cycles (0: default)
   // tracing
   bool profiling = false;
   int32_t launches[UPF_NUM_STAGES] = {};
@@ -349,6 +350,7 @@ upf::ScoreArgs score_args(const upf_ctx* ctx, const upf_batch* b, const Plan& pl
   a.p1part = at<float2>(ws, pl.off_p1);
   a.part = at<float>(ws, pl.off_part);
   a.status = ctx->status_dev;
+  a.wait_limit = ctx->wait_limit > 0 ? ctx->wait_limit : upf::kDefaultWaitCycles;
   for (int i = 0; i < pl.Hq; ++i) a.qhead[i] = pl.qhead[i];
   return a;
 }
@@ -607,9 +609,11 @@ size_t upf_workspace_bytes(const upf_batch* batch, const upf_params* params) {
   return pl.total;
 }
 
-upf_status upf_score(upf_ctx* ctx, const upf_batch* batch, const upf_params* params, const void* q,
-                     int64_t q_row_stride, const void* k, int64_t k_row_stride, float* scores, void* ws,
-                     size_t ws_bytes, void* stream) {
+// upf_score and upf_score_shard: scores normalised by hq_norm q heads (the
+// batch's own H_q, or the total over tensor-parallel ranks).
+static upf_status score_impl(upf_ctx* ctx, const upf_batch* batch, const upf_params* params, int hq_norm,
+                             const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride,
+                             float* scores, void* ws, size_t ws_bytes, void* stream) {
   upf_status st;
   if ((st = check_ctx(ctx)) != UPF_OK) return st;
   Plan pl;
@@ -617,6 +621,8 @@ upf_status upf_score(upf_ctx* ctx, const upf_batch* batch, const upf_params* par
   if ((st = check_ws(pl, ws, ws_bytes)) != UPF_OK) return st;
   if ((st = check_score_io(pl, q, q_row_stride, k, k_row_stride)) != UPF_OK) return st;
   if (!scores) return fail(UPF_ERR_INVALID_ARG, "scores is NULL");
+  if (hq_norm < pl.Hq || hq_norm > (1 << 20))
+    return fail(UPF_ERR_INVALID_ARG, "num_q_heads_total (%d) must be in [num_q_heads (%d), 2^20]", hq_norm, pl.Hq);
   DeviceGuard guard(ctx->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const upf::DescribeArgs da = describe_args(ctx, batch, pl, ws);
@@ -626,7 +632,31 @@ upf_status upf_score(upf_ctx* ctx, const upf_batch* batch, const upf_params* par
   UPF_LAUNCH(staged(ctx, kPass2, s, [&] { return upf::launch_score_pass2(sa, s, true); }), "score pass 2");
   upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC * pl.pw, sa.part, nullptr, scores, nullptr,
                                    nullptr, nullptr);
+  se.Hq = hq_norm;
   UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s, true); }), "finalize scores");
+  return UPF_OK;
+}
+
+upf_status upf_score(upf_ctx* ctx, const upf_batch* batch, const upf_params* params, const void* q,
+                     int64_t q_row_stride, const void* k, int64_t k_row_stride, float* scores, void* ws,
+                     size_t ws_bytes, void* stream) {
+  if (!batch) return fail(UPF_ERR_INVALID_ARG, "batch is NULL");
+  return score_impl(ctx, batch, params, batch->num_q_heads, q, q_row_stride, k, k_row_stride, scores, ws, ws_bytes,
+                    stream);
+}
+
+upf_status upf_score_shard(upf_ctx* ctx, const upf_batch* batch, const upf_params* params,
+                           int32_t num_q_heads_total, const void* q, int64_t q_row_stride, const void* k,
+                           int64_t k_row_stride, float* scores, void* ws, size_t ws_bytes, void* stream) {
+  return score_impl(ctx, batch, params, num_q_heads_total, q, q_row_stride, k, k_row_stride, scores, ws, ws_bytes,
+                    stream);
+}
+
+upf_status upf_set_wait_limit(upf_ctx* ctx, int64_t cycles) {
+  upf_status st = check_ctx(ctx);
+  if (st != UPF_OK) return st;
+  if (cycles < 0) return fail(UPF_ERR_INVALID_ARG, "wait limit must be >= 0 cycles (0 restores the default)");
+  ctx->wait_limit = cycles;
   return UPF_OK;
 }
 

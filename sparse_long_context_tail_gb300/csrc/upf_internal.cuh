@@ -31,6 +31,9 @@ constexpr int kPlanSMs = 152;             // SM count the work split is planned 
 // per pass-1 item row (the epilogue warps that split a unit's columns merge
 // their sums inside the CTA).
 constexpr int kTcPartials = 1;
+// Longest a pipeline wait inside the tensor-core kernels may take by default,
+// in SM clock cycles (about 2 s at 2 GHz).
+constexpr long long kDefaultWaitCycles = 4000000000LL;
 
 struct ScoreArgs {
   const __nv_bfloat16* q;
@@ -51,6 +54,7 @@ struct ScoreArgs {
   float* part;               // [Hkv*NQC*pw][T]
   int32_t pw;                // partial rows per item row / per (g, qc): kTcPartials or 1
   int32_t* status;
+  long long wait_limit;      // pipeline waits of the tensor-core kernels (cycles)
   int32_t qhead[kMaxHeads];  // q heads of group g at [g*gamma, (g+1)*gamma)
 };
 

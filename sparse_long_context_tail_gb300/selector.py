@@ -121,11 +121,15 @@ class TokenSelector:
 
     def score(self, q: torch.Tensor, k: torch.Tensor, cu_seqlens_host: np.ndarray, cu_seqlens_dev: torch.Tensor,
               num_q_heads: int, num_kv_heads: int, head_dim: int, params: Optional[B.UpfParams] = None,
-              kv_of_q: Optional[Sequence[int]] = None, scores: Optional[torch.Tensor] = None) -> torch.Tensor:
+              kv_of_q: Optional[Sequence[int]] = None, scores: Optional[torch.Tensor] = None,
+              total_q_heads: Optional[int] = None) -> torch.Tensor:
         """Token importances alone (``upf_score``): float32 [T] on the selector's GPU.
 
         q and k may be views of a wider tensor (a head range of every row): the
-        row strides are passed through."""
+        row strides are passed through.  With ``total_q_heads`` (a tensor-
+        parallel rank's share of the heads) the scores are normalised by that
+        many q heads (``upf_score_shard``), so the ranks' scores sum to the
+        all-heads score."""
         params = params or B.make_params()
         batch, keep = B.make_batch(cu_seqlens_dev.data_ptr(), cu_seqlens_host, num_q_heads, num_kv_heads,
                                    head_dim, kv_of_q)
@@ -135,8 +139,12 @@ class TokenSelector:
         if scores is None:
             scores = torch.empty(T, dtype=torch.float32, device=self.device)
         stream = torch.cuda.current_stream(self.device).cuda_stream
-        B.upf_score(self.ctx, batch, params, q.data_ptr(), q.stride(0), k.data_ptr(), k.stride(0), scores.data_ptr(),
-                    ws.data_ptr(), ws.numel(), stream)
+        if total_q_heads is None:
+            B.upf_score(self.ctx, batch, params, q.data_ptr(), q.stride(0), k.data_ptr(), k.stride(0),
+                        scores.data_ptr(), ws.data_ptr(), ws.numel(), stream)
+        else:
+            B.upf_score_shard(self.ctx, batch, params, int(total_q_heads), q.data_ptr(), q.stride(0), k.data_ptr(),
+                              k.stride(0), scores.data_ptr(), ws.data_ptr(), ws.numel(), stream)
         del keep
         return scores
 

@@ -6,12 +6,13 @@ own heads, and the per-GPU scores are summed before the keep decision, so all
 GPUs take the same decision and drop the same tokens.
 
 Here rank r of P owns the contiguous kv heads [r H_kv/P, (r+1) H_kv/P) and the
-q heads that read them.  ``upf_score`` on the local heads gives
-s^(r)_k = 1/(H_q/P n_eff) sum_{h of r} ..., so the global score (the average
-over all H_q heads) is the mean of the P local scores.  One all-reduce (sum)
-of the fp32 [T] scores is the only exchange; every rank then runs the same
-selection and compaction on its own copy of the hidden rows.  The all-reduce
-leaves the same bits on every rank, so the masks agree.
+q heads that read them.  ``upf_score_shard`` on the local heads, normalised by
+the total head count H_q, gives s^(r)_k = 1/(H_q n_eff) sum_{h of r} ..., so
+the global score (the average over all H_q heads) is the plain sum of the P
+rank scores.  One sum all-reduce of the fp32 [T] scores is the only exchange
+and the only arithmetic outside the library's kernels is that sum; every rank
+then runs the same selection and compaction on its own copy of the hidden
+rows.  The all-reduce leaves the same bits on every rank, so the masks agree.
 """
 from __future__ import annotations
 
@@ -36,20 +37,19 @@ def shard_heads(num_q_heads: int, num_kv_heads: int, rank: int, world: int) -> T
     return slice(rank * q, (rank + 1) * q), slice(rank * kv, (rank + 1) * kv)
 
 
-def mean_of_partials(partials: Sequence[torch.Tensor]) -> torch.Tensor:
-    """Global scores from the P ranks' local scores, summed in rank order."""
+def sum_of_partials(partials: Sequence[torch.Tensor]) -> torch.Tensor:
+    """Global scores from the P ranks' shard scores, summed in rank order."""
     total = partials[0].clone()
     for p in partials[1:]:
         total += p
-    return total.mul_(1.0 / len(partials))
+    return total
 
 
 def allreduce_scores(local: torch.Tensor, group=None) -> torch.Tensor:
-    """In place: the mean over the group's ranks of their local scores."""
+    """In place: the sum over the group's ranks of their shard scores."""
     import torch.distributed as dist
-    world = dist.get_world_size(group)
     dist.all_reduce(local, op=dist.ReduceOp.SUM, group=group)
-    return local.mul_(1.0 / world)
+    return local
 
 
 def tp_select_tokens(sel: TokenSelector, q_local: torch.Tensor, k_local: torch.Tensor,
@@ -62,18 +62,21 @@ def tp_select_tokens(sel: TokenSelector, q_local: torch.Tensor, k_local: torch.T
     """One full-attention layer's selection on this rank's heads.
 
     q_local / k_local: this rank's head slices ([T, H_q/P, d] / [T, H_kv/P, d],
-    views with the full row strides are fine).  Scores the local heads, averages
-    the scores over the ranks of `group` (one all-reduce), then selects and
-    compacts exactly as the single-GPU call does.  Shapes are checked before
-    the exchange: a rank given the wrong slice raises without entering it, and
-    the other ranks' exchange then fails on the process group's timeout."""
+    views with the full row strides are fine).  Scores the local heads
+    normalised by all H_q = P * local_q_heads heads, sums the scores over the
+    ranks of `group` (one all-reduce), then selects and compacts exactly as the
+    single-GPU call does.  Shapes are checked before the exchange: a rank given
+    the wrong slice raises without entering it, and the other ranks' exchange
+    then fails on the process group's timeout."""
     for name, t, heads in (("q_local", q_local, local_q_heads), ("k_local", k_local, local_kv_heads)):
         if t.dim() != 3 or t.shape[1] != heads or t.shape[2] != head_dim:
             raise ValueError(f"{name} has shape {tuple(t.shape)}, expected [T, {heads}, {head_dim}]")
     if q_local.shape[0] != k_local.shape[0] or q_local.shape[0] != int(cu_seqlens_host[-1]):
         raise ValueError("q_local, k_local and cu_seqlens disagree on the token count")
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
     scores = sel.score(q_local, k_local, cu_seqlens_host, cu_seqlens_dev, local_q_heads, local_kv_heads,
-                       head_dim, params=params)
+                       head_dim, params=params, total_q_heads=world * local_q_heads)
     allreduce_scores(scores, group)
     return sel.select_compact(scores, cu_seqlens_host, cu_seqlens_dev, hidden, positions, slots, layer_id,
                               history, history_len, params, out)

@@ -95,3 +95,11 @@ def test_create_without_gpu_reports_an_error(lib):
 def test_destroy_null_is_an_argument_error(lib):
     assert lib.upf_destroy(None) == 1
     assert "NULL" in B.upf_last_error()
+
+
+def test_wait_limit_and_shard_scoring_check_their_arguments(lib):
+    assert lib.upf_set_wait_limit(None, 100) == 1 and "context" in B.upf_last_error()
+    b, keep = _batch([0, 1000], Hq=8, Hkv=2)
+    with pytest.raises(B.UpfError) as e:
+        B.upf_score_shard(None, b, B.make_params(), 32, 16, 4096, 16, 1024, 16, 256, 1 << 20)
+    assert e.value.status == 1

@@ -335,10 +335,10 @@ def test_compact_spans_several_chunks(sel):
 @pytest.mark.parametrize("name,world", [("ragged-d64", 2), ("llama-2req", 2), ("llama-2req", 4)])
 def test_tensor_parallel_heads_on_one_gpu(sel, name, world):
     """Heads sharded over `world` ranks, run one after another on this GPU:
-    each rank scores its own heads (``upf_score`` on head-range views), the
-    local scores are averaged in rank order (what the all-reduce computes), and
-    selection plus compaction follow.  Everything is checked against the
-    oracle's all-heads result."""
+    each rank scores its own heads (``upf_score_shard`` on head-range views,
+    normalised by all H_q heads), the shard scores are summed in rank order
+    (what the all-reduce computes), and selection plus compaction follow.
+    Everything is checked against the oracle's all-heads result."""
     from sparse_long_context_tail_gb300 import tp
     c = dict(SMALL)[name]
     spec = small_spec("tp-" + name, c)
@@ -351,8 +351,8 @@ def test_tensor_parallel_heads_on_one_gpu(sel, name, world):
     for r in range(world):
         qs, ks = tp.shard_heads(spec.num_q_heads, spec.num_kv_heads, r, world)
         partials.append(sel.score(q[:, qs], k[:, ks], w.cu_seqlens, cu_dev, qs.stop - qs.start, ks.stop - ks.start,
-                                  spec.head_dim, params=p))
-    scores = tp.mean_of_partials(partials)
+                                  spec.head_dim, params=p, total_q_heads=spec.num_q_heads))
+    scores = tp.sum_of_partials(partials)
     hid, pos, slots = _up(w.hidden_bits().view(np.int16)), _up(w.positions()), _up(w.slots())
     out = sel.select_compact(scores, w.cu_seqlens, cu_dev, hid, pos, slots, layer_id=3, params=p)
     torch.cuda.synchronize()

@@ -1,9 +1,9 @@
 """Tensor-parallel score exchange on CPU ranks (gloo, world size 2).
 
-Each rank scores only its own heads (here with the oracle, on the CPU), the
-ranks average their local scores with one all-reduce, and the result must be
-the all-heads score on every rank, bit-identical across ranks, with the same
-selection.  A rank that dies before the exchange makes the other rank's
+Each rank scores only its own heads (here with the oracle, on the CPU,
+normalised by the total head count as ``upf_score_shard`` does), the ranks sum
+their shard scores with one all-reduce, and the result must be the all-heads
+score on every rank, bit-identical across ranks, with the same selection.  A rank that dies before the exchange makes the other rank's
 exchange fail with an error instead of hanging.
 """
 import datetime
@@ -33,10 +33,13 @@ def _spec():
 
 
 def _local_scores(w, rank, world):
+    """The oracle's score over this rank's heads, normalised by all H_q heads
+    (the oracle normalises by the heads it is given: rescale by H_local / H_q)."""
     s = w.spec
     qs, ks = tp.shard_heads(s.num_q_heads, s.num_kv_heads, rank, world)
-    return oracle.token_scores(np.ascontiguousarray(w.k_bits[:, ks]), np.ascontiguousarray(w.q_tail_bits[:, qs]),
-                               w.cu_seqlens, qs.stop - qs.start, ks.stop - ks.start, s.head_dim, s.n_tail)
+    local = oracle.token_scores(np.ascontiguousarray(w.k_bits[:, ks]), np.ascontiguousarray(w.q_tail_bits[:, qs]),
+                                w.cu_seqlens, qs.stop - qs.start, ks.stop - ks.start, s.head_dim, s.n_tail)
+    return local * ((qs.stop - qs.start) / s.num_q_heads)
 
 
 def _exchange_worker(rank, world, port, out):
@@ -67,13 +70,13 @@ def test_shard_heads_covers_every_group_once():
         tp.shard_heads(32, 8, 2, 2)
 
 
-def test_mean_of_partials_is_the_all_heads_score():
+def test_sum_of_shard_scores_is_the_all_heads_score():
     w = wl.generate(_spec())
     s = w.spec
     full = oracle.token_scores(w.k_bits, w.q_tail_bits, w.cu_seqlens, s.num_q_heads, s.num_kv_heads, s.head_dim,
                                s.n_tail)
     for world in (2, 4):
-        got = tp.mean_of_partials([torch.from_numpy(_local_scores(w, r, world)) for r in range(world)]).numpy()
+        got = tp.sum_of_partials([torch.from_numpy(_local_scores(w, r, world)) for r in range(world)]).numpy()
         np.testing.assert_allclose(got, full, rtol=1e-12, atol=1e-300)
 
 
@@ -107,8 +110,8 @@ class _FakeSelector:
         self.local_scores = local_scores
         self.calls = []
 
-    def score(self, q, k, cu_host, cu_dev, hq, hkv, d, params=None):
-        self.calls.append(("score", hq, hkv, d, tuple(q.shape), tuple(k.shape)))
+    def score(self, q, k, cu_host, cu_dev, hq, hkv, d, params=None, total_q_heads=None):
+        self.calls.append(("score", hq, hkv, d, tuple(q.shape), tuple(k.shape), total_q_heads))
         return self.local_scores.clone()
 
     def select_compact(self, scores, cu_host, cu_dev, hidden, positions, slots, layer_id, history, history_len,
@@ -133,7 +136,7 @@ def _glue_worker(rank, world, port, out):
         dist.destroy_process_group()
 
 
-def test_tp_select_tokens_scores_locally_then_selects_on_the_mean():
+def test_tp_select_tokens_scores_locally_then_selects_on_the_sum():
     ctx = mp.get_context("spawn")
     mgr = ctx.Manager()
     out = mgr.dict()
@@ -146,10 +149,10 @@ def test_tp_select_tokens_scores_locally_then_selects_on_the_mean():
         assert p.exitcode == 0
     (b0, c0), (b1, c1) = out[0], out[1]
     assert b0 == b1
-    want = (np.arange(50, dtype=np.float32) * 1.5)          # mean of 1x and 2x the local scores
+    want = (np.arange(50, dtype=np.float32) * 3.0)          # sum of 1x and 2x the shard scores
     np.testing.assert_array_equal(np.frombuffer(b0, dtype=np.float32), want)
     for calls in (c0, c1):
-        assert calls == [("score", 4, 2, 64, (50, 4, 64), (50, 2, 64)), ("select_compact", 7)]
+        assert calls == [("score", 4, 2, 64, (50, 4, 64), (50, 2, 64), 8), ("select_compact", 7)]
 
 
 def test_tp_select_tokens_rejects_a_wrong_head_slice_before_any_exchange():
