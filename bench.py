@@ -66,6 +66,10 @@ def parse_args():
     ap.add_argument("--no-gather-p1", action="store_true", help="skip the supplementary all-kept gather point")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip timing the other benchmark workloads after the headline one")
+    ap.add_argument("--tp", action="store_true",
+                    help="tensor-parallel mode: heads sharded over the ranks, one score all-reduce per step")
     return ap.parse_args()
 
 
@@ -211,23 +215,16 @@ class ClockSampler:
 
 # ------------------------------------------------------------ CPU oracle ----
 
-def oracle_run(w, heads=None, threads=None):
-    """One pass of the float64 oracle over the workload (optionally a subset of q-heads for scoring).
+def oracle_run(w, threads=None):
+    """One whole pass of the float64 oracle over the workload.
 
     Returns (score seconds, rest seconds, threads used)."""
     import oracle
     s = w.spec
     thr = threads or min(32, os.cpu_count() or 1)
     t0 = time.perf_counter()
-    if heads is None or heads >= s.num_q_heads:
-        scores = oracle.token_scores(w.k_bits, w.q_tail_bits, w.cu_seqlens, s.num_q_heads, s.num_kv_heads,
-                                     s.head_dim, s.n_tail, None, s.kv_of_q, thr)
-    else:
-        # the first `heads` q-heads (their kv heads follow the group map): a sample of the per-head work
-        gmap = s.group_map()
-        q = w.q_tail_bits[:, :heads, :]
-        scores = oracle.token_scores(w.k_bits, q, w.cu_seqlens, heads, s.num_kv_heads, s.head_dim, s.n_tail,
-                                     None, gmap[:heads].tolist(), thr)
+    scores = oracle.token_scores(w.k_bits, w.q_tail_bits, w.cu_seqlens, s.num_q_heads, s.num_kv_heads,
+                                 s.head_dim, s.n_tail, None, s.kv_of_q, thr)
     t1 = time.perf_counter()
     sel = oracle.select(scores, w.cu_seqlens, s.block, s.top_p, s.sink_keep, s.tail_keep)
     oracle.compact(sel["mask"], w.cu_seqlens, w.hidden_bits(), w.positions(), w.slots(), 0)
@@ -253,6 +250,10 @@ def cpu_baseline(w, budget_s=15.0):
 
 
 def run_reference(args):
+    """The baseline arm: the float64 oracle as it stands, whole passes over the
+    workload on the host cores (each step is one complete pass: scores of
+    every q-head and tail query, block means, top-p + exempt mask, compaction
+    with the hidden rows, positions and slots)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
@@ -261,21 +262,18 @@ def run_reference(args):
         spec.top_p = args.top_p
     w = wl.generate(spec)
     w.hidden_bits()
-    # Each step scores a sample of q-heads (the per-head work scales linearly) and
-    # runs selection + compaction in full; sized so warmup + steps stay within ~3 min.
-    t_score_1head, _, thr = oracle_run(w, heads=1)
-    per_step_budget = 150.0 / max(1, args.steps + args.warmup)
-    heads = int(max(1, min(spec.num_q_heads, per_step_budget / max(t_score_1head, 1e-3))))
+    thr = None
     for _ in range(args.warmup):
-        oracle_run(w, heads=heads)
-    est = []
+        oracle_run(w)
+    per_step = []
     for _ in range(args.steps):
-        ts, tr, thr = oracle_run(w, heads=heads)
-        est.append(ts * spec.num_q_heads / heads + tr)
-    per = statistics.mean(est)
+        ts, tr, thr = oracle_run(w)
+        per_step.append(ts + tr)
+    per = statistics.mean(per_step)
     value = w.total_tokens / per
-    sample = (f"each step: float64 oracle scoring of {heads} of {spec.num_q_heads} q-heads (time scaled by "
-              f"{spec.num_q_heads}/{heads}) plus full selection and compaction of {spec.name}")
+    sample = (f"each step: one whole pass of the float64 oracle over {spec.name} ({w.total_tokens} tokens, all "
+              f"{spec.num_q_heads} q-heads and {spec.n_tail} tail queries, selection and compaction); "
+              f"{args.steps} timed passes after {args.warmup} untimed, mean {per:.2f} s per pass")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -287,12 +285,173 @@ def run_reference(args):
 
 
 def config_of(spec, w, args):
+    tp_mode = getattr(args, "tp", False)
     return {"workload": spec.name, "requests": len(spec.lengths), "total_tokens": w.total_tokens,
             "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim,
             "hidden": spec.hidden, "n_tail": spec.n_tail, "block": spec.block, "top_p": spec.top_p,
             "sink_keep": spec.sink_keep, "tail_keep": spec.tail_keep,
             "l2": "flushed between steps (512 MiB write)" if not args.no_flush else "not flushed",
-            "parallelism": f"replicas x{args.gpus} (requests sharded per GPU, no collective)"}
+            "parallelism": (f"tp{args.gpus} (heads sharded over ranks, one sum all-reduce of the fp32 scores)"
+                            if tp_mode else f"replicas x{args.gpus} (requests sharded per GPU, no collective)")}
+
+
+# -------------------------------------------------------------- rooflines ----
+
+def scoring_bound(work_stage, peaks):
+    """'tensor' when the pass's arithmetic intensity (flop per DRAM byte of K
+    and tail Q) is above the ridge of the measured peaks, else 'hbm'."""
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    return "tensor" if work_stage["flops"] / max(1.0, work_stage["bytes"]) >= ridge else "hbm"
+
+
+def kernel_roofline(stage, work, sec_per_launch, peaks, peak_kind, workload_name):
+    """Roofline entry of one kernel: algorithmic work per launch / its mean
+    launch time, against the measured peak of the unit that bounds it.
+
+    The scoring passes are timed alone (one launch of well under a
+    millisecond), so a tensor-bound pass takes the burst bf16 peak; the
+    sustained figure is given beside it, labelled."""
+    wk = work[stage]
+    if stage in ("score_pass1", "score_pass2"):
+        bound = scoring_bound(wk, peaks)
+    else:
+        bound = "hbm"
+    if bound == "tensor":
+        achieved = wk["flops"] / sec_per_launch / 1e12
+        peak, unit, key = peaks["bf16_tflops"], "TFLOP/s", "bf16_tflops"
+    else:
+        achieved = wk["bytes"] / sec_per_launch / 1e9
+        peak, unit, key = peaks["hbm_gbs"], "GB/s", "hbm_gbs"
+    r = {"bound": bound, "kernel": stage, "achieved": achieved, "peak": peak, "unit": unit,
+         "frac": achieved / peak, "peak_source": f"{peak_kind} {key}" + (" (burst)" if bound == "tensor" else ""),
+         "traffic": traffic_record(stage, workload_name), "us_per_launch": sec_per_launch * 1e6,
+         "algorithmic_bytes_per_launch": wk["bytes"]}
+    if "flops" in wk:
+        r["algorithmic_flops_per_launch"] = wk["flops"]
+        r["tflops"] = wk["flops"] / sec_per_launch / 1e12
+        r["gbs"] = wk["bytes"] / sec_per_launch / 1e9
+        if bound == "tensor" and "bf16_tflops_sustained" in peaks:
+            r["frac_of_sustained_peak"] = achieved / peaks["bf16_tflops_sustained"]
+    return r
+
+
+# ------------------------------------------------------------ one workload ----
+
+class DeviceInputs:
+    """A workload's inputs resident in HBM (the tail Q rows inside a [T, H_q, d]
+    tensor, K, hidden rows, positions, slot ids, cu_seqlens)."""
+
+    def __init__(self, torch, w, dev, hidden_from_host=True):
+        spec = w.spec
+        T = w.total_tokens
+        self.q = torch.zeros((T, spec.num_q_heads, spec.head_dim), dtype=torch.bfloat16, device=dev)
+        q_tail = torch.from_numpy(w.q_tail_bits.view(np.int16)).view(torch.bfloat16)
+        self.q[torch.from_numpy(w.tail_rows).to(dev)] = q_tail.to(dev)
+        self.k = torch.from_numpy(w.k_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+        if hidden_from_host:
+            self.hidden = torch.from_numpy(w.hidden_bits().view(np.int16)).to(dev)
+        else:   # contents do not affect the path (bit-copied rows): device zeros, no host generation
+            self.hidden = torch.zeros((T, spec.hidden), dtype=torch.int16, device=dev)
+        self.pos = torch.from_numpy(w.positions()).to(dev)
+        self.slot = torch.from_numpy(w.slots()).to(dev)
+        self.cu = torch.from_numpy(w.cu_seqlens).to(dev)
+
+
+def timed_loop(torch, fn, stream, steps, flush):
+    """Per-step device ms of `steps` calls of fn, CUDA events on `stream`, L2
+    flushed between steps (outside the events)."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+        if flush is not None:
+            flush.zero_()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
+def traced_loop(torch, B, sel, fn, stream, steps, flush):
+    """The same steps with an event pair around every launch (library tracing):
+    per-stage launches and summed ms, plus the traced step times."""
+    B.upf_profile_read(sel.ctx)
+    B.upf_profile_enable(sel.ctx, True)
+    traced = timed_loop(torch, fn, stream, steps, flush)
+    launches, stage_ms = B.upf_profile_read(sel.ctx)
+    B.upf_profile_enable(sel.ctx, False)
+    return launches, stage_ms, traced
+
+
+def stage_table(work, launches, stage_ms):
+    tot_ms = sum(stage_ms) or 1.0
+    stages = {}
+    for i, nm in enumerate(STAGES):
+        n_l = max(1, launches[i])
+        per = stage_ms[i] / n_l
+        entry = {"launches": launches[i], "ms_per_launch": per, "share": stage_ms[i] / tot_ms}
+        wk = work[nm]
+        if per > 0:
+            if "flops" in wk:
+                entry["tflops"] = wk["flops"] / (per / 1e3) / 1e12
+            entry["gbs"] = wk["bytes"] / (per / 1e3) / 1e9
+        stages[nm] = entry
+    return stages
+
+
+def run_per_config(torch, B, sel, names, dev, stream, flush, peaks, peak_kind, steps=10, warmup=3):
+    """tokens/s, per-stage us and the scoring passes' roofline fractions of the
+    other benchmark workloads (the headline line measures only its own).
+    Inputs are the seeded workloads (hidden rows are device zeros: the path
+    bit-copies them, so their values change nothing but are never read as
+    numbers)."""
+    out = {}
+    for name in names:
+        t0 = time.time()
+        spec = wl.named_spec(name)
+        w = wl.generate(spec)
+        x = DeviceInputs(torch, w, dev, hidden_from_host=False)
+        cu = w.cu_seqlens
+        params = B.make_params(spec.n_tail, spec.block, spec.sink_keep, spec.tail_keep, spec.top_p)
+        o = sel.alloc_outputs(cu, spec.block, x.hidden, x.pos, x.slot)
+
+        def step(o=o, x=x, spec=spec, cu=cu, params=params):
+            return sel.select_tokens(x.q, x.k, cu, x.cu, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                                     x.hidden, x.pos, x.slot, layer_id=0, params=params, kv_of_q=spec.kv_of_q,
+                                     out=o)
+
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        status = sel.status()
+        kept = int(o.total_kept.item())
+        ms = timed_loop(torch, step, stream, steps, flush)
+        launches, stage_ms, _ = traced_loop(torch, B, sel, step, stream, steps, flush)
+        graph = graph_replay(torch, step, stream, steps, flush)
+        T = w.total_tokens
+        work = algorithmic_work(spec, cu, kept, x.hidden.stride(0) * 2, spec.top_p)
+        entry = {"tokens": T, "requests": len(spec.lengths), "ms_per_step": statistics.mean(ms),
+                 "median_ms": statistics.median(ms), "tokens_per_s": T / (statistics.mean(ms) / 1e3),
+                 "graph_ms_per_step": graph["ms_per_step"], "kept_tokens": kept, "kept_fraction": kept / T,
+                 "status": B.STATUS_NAMES.get(status, status),
+                 "stage_us": {nm: 1e3 * stage_ms[i] / max(1, launches[i]) for i, nm in enumerate(STAGES)
+                              if launches[i]},
+                 "stage_sum_us": 1e3 * sum(stage_ms) / steps}
+        for nm in ("score_pass1", "score_pass2"):
+            i = STAGES.index(nm)
+            if launches[i] and stage_ms[i] > 0:
+                rf = kernel_roofline(nm, work, stage_ms[i] / launches[i] / 1e3, peaks, peak_kind, name)
+                entry[nm] = {k: rf[k] for k in ("bound", "achieved", "unit", "frac", "tflops", "gbs",
+                                                "us_per_launch")}
+        out[name] = entry
+        log(f"[bench] per-config {name}: {entry['ms_per_step'] * 1e3:.1f} us/step "
+            f"({time.time() - t0:.1f} s incl. generation)")
+        del x, o, w
+        torch.cuda.empty_cache()
+    return out
+
+
+PER_CONFIG = ["small-L4096", "llama8b-L32768", "llama8b-batch16"] + list(wl.SWEEP_NAMES)
 
 
 # ----------------------------------------------------------------- ours -----
@@ -303,6 +462,8 @@ def main():
         return run_reference(args)
     if args.stack:
         return run_stack(args)
+    if args.tp:
+        return run_tp(args)
     import torch
     import torch.distributed as dist
 
@@ -323,22 +484,14 @@ def main():
         spec.top_p = args.top_p
     t0 = time.time()
     w = wl.generate(spec)
-    hidden_np = w.hidden_bits()
+    w.hidden_bits()
     log(f"[bench] generated {spec.name} in {time.time() - t0:.1f} s")
     cu = w.cu_seqlens
     T = w.total_tokens
     params = B.make_params(spec.n_tail, spec.block, spec.sink_keep, spec.tail_keep, spec.top_p)
 
-    # inputs resident in HBM
-    q_dev = torch.empty((T, spec.num_q_heads, spec.head_dim), dtype=torch.bfloat16, device=dev)
-    q_tail = torch.from_numpy(w.q_tail_bits.view(np.int16)).view(torch.bfloat16)
-    tail_idx = torch.from_numpy(w.tail_rows)
-    q_dev[tail_idx.to(dev)] = q_tail.to(dev)
-    k_dev = torch.from_numpy(w.k_bits.view(np.int16)).to(dev).view(torch.bfloat16)
-    hid_dev = torch.from_numpy(hidden_np.view(np.int16)).to(dev)
-    pos_dev = torch.from_numpy(w.positions()).to(dev)
-    slot_dev = torch.from_numpy(w.slots()).to(dev)
-    cu_dev = torch.from_numpy(cu).to(dev)
+    x = DeviceInputs(torch, w, dev)          # inputs resident in HBM
+    q_dev, k_dev, hid_dev, pos_dev, slot_dev, cu_dev = x.q, x.k, x.hidden, x.pos, x.slot, x.cu
     sel = TokenSelector(local)
     out = sel.alloc_outputs(cu, spec.block, hid_dev, pos_dev, slot_dev)
     flush = None if args.no_flush else torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -357,8 +510,6 @@ def main():
     kept_total = int(out.total_kept.item())
 
     stream = torch.cuda.current_stream(dev)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -369,29 +520,11 @@ def main():
     # Headline loop: tracing off, so consecutive kernels of a step overlap
     # their launch with the predecessor's tail (programmatic dependent launch).
     wall0 = time.perf_counter()
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-        if flush is not None:
-            flush.zero_()
-    torch.cuda.synchronize()
+    step_ms = timed_loop(torch, step, stream, args.steps, flush)
     wall = time.perf_counter() - wall0
     launches, _ = B.upf_profile_read(sel.ctx)
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     # Breakdown loop: the same steps with an event pair around every launch.
-    B.upf_profile_enable(sel.ctx, True)
-    traced = []
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-        if flush is not None:
-            flush.zero_()
-    torch.cuda.synchronize()
-    traced = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    _, stage_ms = B.upf_profile_read(sel.ctx)
-    B.upf_profile_enable(sel.ctx, False)
+    _, stage_ms, traced = traced_loop(torch, B, sel, step, stream, args.steps, flush)
     # The same step captured once in a CUDA graph and replayed (launches keep
     # their programmatic-dependent-launch edges inside the graph).
     graph = None
@@ -403,41 +536,19 @@ def main():
     sec, _, value = aggregate_over_ranks(statistics.mean(step_ms) / 1e3, T, dist if world > 1 else None, dev)
     ms = sec * 1e3
 
-    # roofline of the dominant kernel (largest share of device time)
+    # roofline of the dominant kernel (largest share of device time), and of both scoring passes
     work = algorithmic_work(spec, cu, kept_total, hid_dev.stride(0) * 2, spec.top_p)
     peaks, peak_kind = load_peaks()
-    tot_ms = sum(stage_ms) or 1.0
-    stages = {}
-    for i, nm in enumerate(STAGES):
-        n_l = max(1, launches[i])
-        per = stage_ms[i] / n_l
-        entry = {"launches": launches[i], "ms_per_launch": per, "share": stage_ms[i] / tot_ms}
-        wk = work[nm]
-        if per > 0:
-            if "flops" in wk:
-                entry["tflops"] = wk["flops"] / (per / 1e3) / 1e12
-            entry["gbs"] = wk["bytes"] / (per / 1e3) / 1e9
-        stages[nm] = entry
+    stages = stage_table(work, launches, stage_ms)
     dom = max(range(len(STAGES)), key=lambda i: stage_ms[i])
-    dname = STAGES[dom]
-    dwork = work[dname]
-    dper = stage_ms[dom] / max(1, launches[dom]) / 1e3
-    if dwork["bound"] == "tensor":
-        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-        achieved = dwork["flops"] / dper / 1e12
-        unit = "TFLOP/s"
-    else:
-        peak = peaks["hbm_gbs"]
-        achieved = dwork["bytes"] / dper / 1e9
-        unit = "GB/s"
-    traffic = traffic_record(dname, spec.name)
-    roofline = {"bound": "tensor" if dwork["bound"] == "tensor" else "hbm", "kernel": dname,
-                "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                "peak_source": f"{peak_kind} ({'bf16_tflops_sustained' if unit == 'TFLOP/s' else 'hbm_gbs'})",
-                "traffic": traffic}
-    if dwork["bound"] == "tensor":
-        roofline["algorithmic_flops_per_launch"] = dwork["flops"]
-    roofline["algorithmic_bytes_per_launch"] = dwork["bytes"]
+    roofline = kernel_roofline(STAGES[dom], work, stage_ms[dom] / max(1, launches[dom]) / 1e3, peaks, peak_kind,
+                               spec.name)
+    roofline["passes"] = {}
+    for nm in ("score_pass1", "score_pass2"):
+        i = STAGES.index(nm)
+        if launches[i]:
+            roofline["passes"][nm] = kernel_roofline(nm, work, stage_ms[i] / launches[i] / 1e3, peaks, peak_kind,
+                                                     spec.name)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -449,6 +560,14 @@ def main():
     gather_p1 = None
     if not args.no_gather_p1:
         gather_p1 = run_gather_p1(torch, sel, spec, w, cu, cu_dev, hid_dev, pos_dev, slot_dev, out, peaks)
+
+    # the other workloads (one GPU only: they are not the headline)
+    per_config = None
+    if rank == 0 and world == 1 and not args.no_per_config:
+        del x
+        torch.cuda.empty_cache()
+        names = [n for n in PER_CONFIG if n != spec.name]
+        per_config = run_per_config(torch, B, sel, names, dev, stream, flush, peaks, peak_kind)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -463,13 +582,120 @@ def main():
                             "traced_mean": statistics.mean(traced), "stage_sum": sum(stage_ms) / args.steps},
                 "kept_tokens": kept_total, "kept_fraction": kept_total / T,
                 "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e, "gather_p1": gather_p1,
-                "graph": graph,
+                "graph": graph, "per_config": per_config,
                 "gpu_launches": int(sum(launches)), "clocks": clk, "wall_s": wall}
         print(json.dumps(line), flush=True)
     sel.close()
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+# --------------------------------------------------- tensor-parallel mode ----
+
+def tp_shard_inputs(w, rank, world):
+    """This rank's head slices of a workload: (q-head slice, kv-head slice,
+    tail Q bits [n_rows, H_q/P, d], K bits [T, H_kv/P, d])."""
+    from sparse_long_context_tail_gb300 import tp
+    s = w.spec
+    qs, ks = tp.shard_heads(s.num_q_heads, s.num_kv_heads, rank, world)
+    return qs, ks, np.ascontiguousarray(w.q_tail_bits[:, qs]), np.ascontiguousarray(w.k_bits[:, ks])
+
+
+def tp_masks_agree(keep_bits, dist_mod, group=None):
+    """True when every rank of the group holds the same keep mask (all-gather
+    of the mask words, compared on every rank)."""
+    import torch
+    if not (dist_mod.is_available() and dist_mod.is_initialized()) or dist_mod.get_world_size(group) == 1:
+        return True
+    world = dist_mod.get_world_size(group)
+    gathered = [torch.empty_like(keep_bits) for _ in range(world)]
+    dist_mod.all_gather(gathered, keep_bits, group=group)
+    return all(torch.equal(gathered[0], g) for g in gathered[1:])
+
+
+def run_tp(args):
+    """Tensor-parallel selection: the heads of one batch sharded over N ranks
+    (rank r holds only its q and kv heads), each rank scores its heads, one
+    sum all-reduce of the fp32 [T] scores over NCCL, then every rank selects
+    and compacts its own copy of the hidden rows.  The total work is fixed
+    (strong scaling); value = tokens of the batch / the slowest rank's step."""
+    import torch
+    import torch.distributed as dist
+    from sparse_long_context_tail_gb300 import _binding as B
+    from sparse_long_context_tail_gb300 import tp
+    from sparse_long_context_tail_gb300.selector import TokenSelector
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    spec = wl.named_spec(args.workload)
+    if args.top_p is not None:
+        spec.top_p = args.top_p
+    w = wl.generate(spec)                     # the same batch on every rank
+    qs, ks, q_bits, k_bits = tp_shard_inputs(w, rank, world)
+    hq_l, hkv_l = qs.stop - qs.start, ks.stop - ks.start
+    T = w.total_tokens
+    q_local = torch.zeros((T, hq_l, spec.head_dim), dtype=torch.bfloat16, device=dev)
+    q_local[torch.from_numpy(w.tail_rows).to(dev)] = torch.from_numpy(q_bits.view(np.int16)).view(
+        torch.bfloat16).to(dev)
+    k_local = torch.from_numpy(k_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    hid = torch.from_numpy(w.hidden_bits().view(np.int16)).to(dev)
+    pos = torch.from_numpy(w.positions()).to(dev)
+    slot = torch.from_numpy(w.slots()).to(dev)
+    cu = w.cu_seqlens
+    cu_dev = torch.from_numpy(cu).to(dev)
+    params = B.make_params(spec.n_tail, spec.block, spec.sink_keep, spec.tail_keep, spec.top_p)
+    sel = TokenSelector(local)
+    out = sel.alloc_outputs(cu, spec.block, hid, pos, slot)
+    flush = None if args.no_flush else torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        return tp.tp_select_tokens(sel, q_local, k_local, cu, cu_dev, hq_l, hkv_l, spec.head_dim, hid, pos, slot,
+                                   layer_id=0, params=params, out=out)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    status = sel.status()
+    if status != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES.get(status)} during warm-up")
+    agree = tp_masks_agree(out.keep_bits, dist)
+    stream = torch.cuda.current_stream(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    B.upf_profile_read(sel.ctx)
+    step_ms = timed_loop(torch, step, stream, args.steps, flush)
+    launches, _ = B.upf_profile_read(sel.ctx)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    sec = statistics.mean(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([sec], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        sec = float(t.item())
+    kept = int(out.total_kept.item())
+    if rank == 0:
+        line = {"metric": METRIC, "value": T / sec, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "strong",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded bf16 N(0,1) + planted blocks)",
+                "mode": "tp", "config": config_of(spec, w, args), "masks_agree_across_ranks": agree,
+                "kept_tokens": kept, "kept_fraction": kept / T, "allreduce_bytes_per_step": 4 * T,
+                "gpu_launches": int(sum(launches)), "clocks": clk}
+        print(json.dumps(line), flush=True)
+    sel.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0 if agree else 1
 
 
 def graph_replay(torch, step, stream, steps, flush):

@@ -45,10 +45,19 @@ def sum_of_partials(partials: Sequence[torch.Tensor]) -> torch.Tensor:
     return total
 
 
+def _group_size(group=None) -> int:
+    """Ranks in `group`; 1 when no process group is running (a single GPU)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return 1
+    return dist.get_world_size(group)
+
+
 def allreduce_scores(local: torch.Tensor, group=None) -> torch.Tensor:
     """In place: the sum over the group's ranks of their shard scores."""
     import torch.distributed as dist
-    dist.all_reduce(local, op=dist.ReduceOp.SUM, group=group)
+    if _group_size(group) > 1:
+        dist.all_reduce(local, op=dist.ReduceOp.SUM, group=group)
     return local
 
 
@@ -73,8 +82,7 @@ def tp_select_tokens(sel: TokenSelector, q_local: torch.Tensor, k_local: torch.T
             raise ValueError(f"{name} has shape {tuple(t.shape)}, expected [T, {heads}, {head_dim}]")
     if q_local.shape[0] != k_local.shape[0] or q_local.shape[0] != int(cu_seqlens_host[-1]):
         raise ValueError("q_local, k_local and cu_seqlens disagree on the token count")
-    import torch.distributed as dist
-    world = dist.get_world_size(group)
+    world = _group_size(group)
     scores = sel.score(q_local, k_local, cu_seqlens_host, cu_seqlens_dev, local_q_heads, local_kv_heads,
                        head_dim, params=params, total_q_heads=world * local_q_heads)
     allreduce_scores(scores, group)
