@@ -357,12 +357,23 @@ class DeviceInputs:
         self.cu = torch.from_numpy(w.cu_seqlens).to(dev)
 
 
-def timed_loop(torch, fn, stream, steps, flush):
+LEAD_CYCLES = 400000   # ~0.2 ms of GPU sleep before each timed step
+
+
+def timed_loop(torch, fn, stream, steps, flush, lead_cycles=LEAD_CYCLES):
     """Per-step device ms of `steps` calls of fn, CUDA events on `stream`, L2
-    flushed between steps (outside the events)."""
+    flushed between steps (outside the events).
+
+    Before each step's start event the stream sleeps for `lead_cycles` GPU
+    cycles (a bounded sleep kernel): meanwhile the host enqueues the step, so
+    the events time the step's kernels on the device rather than the host's
+    launch path catching up with an idle GPU (the end-to-end figure carries
+    the host path)."""
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for i in range(steps):
+        if lead_cycles:
+            torch.cuda._sleep(lead_cycles)
         starts[i].record(stream)
         fn()
         ends[i].record(stream)
@@ -717,6 +728,7 @@ def graph_replay(torch, step, stream, steps, flush):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     cur = torch.cuda.current_stream()
     for i in range(steps):
+        torch.cuda._sleep(LEAD_CYCLES)   # the replay is enqueued before its start event is reached
         starts[i].record(cur)
         g.replay()
         ends[i].record(cur)

@@ -166,6 +166,14 @@ upf_status upf_sync_status(upf_ctx* ctx, void* stream);
  * on exit are unspecified; it must be 256-byte aligned. */
 size_t upf_workspace_bytes(const upf_batch* batch, const upf_params* params);
 
+/* Work split of the two scoring passes for this batch (inspection and tests;
+ * no GPU needed): keys per split of pass 1 and pass 2 and the number of work
+ * items (one CTA each) of each pass.  Any output may be NULL.  The tensor-core
+ * passes run one CTA per SM, so the split is chosen by the estimated time of
+ * the items over the device's 152 SMs.  Errors: as upf_workspace_bytes. */
+upf_status upf_plan_info(const upf_batch* batch, const upf_params* params, int32_t* key_split1, int32_t* key_split2,
+                         int64_t* items1, int64_t* items2);
+
 /* Tail-query importance of every token (section 二, first step; section 三,
  * scores + online normalisation):
  *   s_k = 1/(H_q * n_eff) * sum_h sum_{j : t_j >= k} softmax_j(k),

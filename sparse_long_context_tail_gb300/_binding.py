@@ -61,6 +61,8 @@ _SIGNATURES = {
     "upf_score_shard": ([c_void_p, POINTER(UpfBatch), POINTER(UpfParams), c_int32, c_void_p, c_int64, c_void_p,
                          c_int64, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
     "upf_set_wait_limit": ([c_void_p, c_int64], c_int),
+    "upf_plan_info": ([POINTER(UpfBatch), POINTER(UpfParams), POINTER(c_int32), POINTER(c_int32), POINTER(c_int64),
+                       POINTER(c_int64)], c_int),
     "upf_select": ([c_void_p, POINTER(UpfBatch), POINTER(UpfParams), c_void_p, c_void_p, c_void_p, c_void_p,
                     c_void_p, c_size_t, c_void_p], c_int),
     "upf_compact": ([c_void_p, POINTER(UpfBatch), c_void_p, POINTER(UpfCompactIO), c_void_p, c_size_t, c_void_p],
@@ -182,6 +184,14 @@ def upf_score_shard(ctx, batch, params, num_q_heads_total, q, q_row_stride, k, k
                     stream=0):
     _check(load().upf_score_shard(ctx, ctypes.byref(batch), ctypes.byref(params), num_q_heads_total, q, q_row_stride,
                                   k, k_row_stride, scores, ws, ws_bytes, stream or None))
+
+
+def upf_plan_info(batch: UpfBatch, params: UpfParams):
+    """(keys per split of pass 1, of pass 2, items of pass 1, items of pass 2)."""
+    k1, k2, i1, i2 = c_int32(), c_int32(), c_int64(), c_int64()
+    _check(load().upf_plan_info(ctypes.byref(batch), ctypes.byref(params), ctypes.byref(k1), ctypes.byref(k2),
+                                ctypes.byref(i1), ctypes.byref(i2)))
+    return k1.value, k2.value, i1.value, i2.value
 
 
 def upf_set_wait_limit(ctx: int, cycles: int) -> None:

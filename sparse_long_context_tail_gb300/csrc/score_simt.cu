@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(32) describe_kernel(const DescribeArgs a) {
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x;
+  for (int i = lane; i < a.ncounters; i += 32) a.counters[i] = 0;
   bool bad = lane == 0 && (a.cu[0] != 0 || a.cu[a.R] != a.T);
   int carry[3] = {0, 0, 0};
   for (int base = 0; base < a.R; base += 32) {

@@ -1,0 +1,282 @@
+// The per-request top-p block selection shared by the selection kernels.
+//
+// UniPrefill article, section 二 second step: rank the blocks by their mean
+// token importance and keep the smallest set whose importance sum reaches p
+// of the total; exemption paragraph: blocks covering the first and last 128
+// tokens are always kept.
+//
+// One CTA (kSelThreads threads) selects one request's blocks.  Block masses
+// become 48-bit fixed-point integers relative to the request's largest block,
+// so totals and histograms are exact integer sums (deterministic in any
+// order; rounding below 1e-10 of the total).  Non-negative float bit patterns
+// order like the values, so an MSB-first radix select over the 32-bit
+// patterns (8 bits per round, integer mass histograms in shared memory) finds
+// the score v* of the last block needed; blocks above v* are in, blocks equal
+// to v* enter in index order until the mass is reached.  No sort.
+//
+// Histogram updates are aggregated per warp before the shared-memory atomic:
+// the blocks of a request have similar magnitudes, so in the first rounds most
+// of them share a few digits, and one atomic per block would serialise on
+// those few addresses.  Lanes with equal digits (match.any) sum their masses
+// with two 32-bit warp reductions (24-bit halves, so no sum overflows) and one
+// lane adds the group's total.
+#pragma once
+
+#include <cmath>
+
+#include "upf_internal.cuh"
+
+namespace upf {
+
+constexpr int kSelThreads = 1024;
+constexpr int kSelWarps = kSelThreads / 32;
+
+// Shared memory the select core needs beyond its static arrays, for a request
+// of up to nbp blocks (nbp a multiple of 8).
+__host__ __device__ constexpr size_t select_smem_bytes(int nbp) {
+  return size_t(nbp) * (sizeof(unsigned long long) + sizeof(uint32_t) + 1);
+}
+
+struct SelectScratch {
+  unsigned long long* m;   // [nbp] fixed-point masses
+  uint32_t* bits;          // [nbp] float bits of the block scores
+  unsigned char* keep;     // [nbp] 1 = kept
+};
+
+__device__ __forceinline__ SelectScratch carve_select(unsigned char* dyn, int nbp) {
+  SelectScratch s;
+  s.m = reinterpret_cast<unsigned long long*>(dyn);
+  s.bits = reinterpret_cast<uint32_t*>(s.m + nbp);
+  s.keep = reinterpret_cast<unsigned char*>(s.bits + nbp);
+  return s;
+}
+
+// 2^e as a float, for e in [-126, 127].
+__device__ __forceinline__ float sel_pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// Block masses as 48-bit fixed point relative to the largest block of the
+// request: m = floor(v * 2^(48 - ex)) with vmax = f * 2^ex, f in [0.5, 1), so
+// every m < 2^48 and a request's total (<= 16384 blocks) stays below 2^62.
+// The scaling is by powers of two only (two steps keep each factor normal).
+__device__ __forceinline__ unsigned long long fixed_mass(float v, int sh) {
+  const int s1 = min(sh, 127);
+  return __float2ull_rz((v * sel_pow2f(s1)) * sel_pow2f(sh - s1));
+}
+
+template <typename T>
+__device__ __forceinline__ T sel_block_sum(T v, T* s_tmp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) s_tmp[warp] = v;
+  __syncthreads();
+  T t = 0;
+  for (int w = 0; w < kSelWarps; ++w) t += s_tmp[w];   // fixed order
+  __syncthreads();
+  return t;
+}
+
+// Adds `mass` to hist[digit] for every lane with digit < 256, one shared
+// atomic per distinct digit of the warp.  Every lane of the warp must call it
+// (lanes with nothing to add pass digit >= 256 and a distinct value each).
+__device__ __forceinline__ void hist_add_aggregated(unsigned long long* hist, uint32_t digit,
+                                                    unsigned long long mass) {
+  const unsigned peers = __match_any_sync(0xffffffffu, digit);
+  const uint32_t lo = __reduce_add_sync(peers, uint32_t(mass & 0xFFFFFFull));
+  const uint32_t hi = __reduce_add_sync(peers, uint32_t(mass >> 24));
+  const int lane = threadIdx.x & 31;
+  if (digit < 256u && lane == __ffs(peers) - 1)
+    atomicAdd(&hist[digit], (unsigned long long)lo + ((unsigned long long)hi << 24));
+}
+
+// Selects the blocks of one request: block scores bs[0..nb) (global, any
+// state space the CTA can read), L tokens.  On return (after a barrier)
+// sc.keep[i] says whether block i is kept (top-p set or exempt) and the
+// kept-token count is returned to every thread.  A NaN, infinite or negative
+// score keeps the whole request and records UPF_ERR_NONFINITE.
+static __device__ int select_request(const float* bs, int nb, int L, int G, float top_p, int sink_keep, int tail_keep,
+                              const SelectScratch& sc, int32_t* status) {
+  __shared__ unsigned long long h_mass[256];
+  __shared__ unsigned long long s_u64[kSelWarps];
+  __shared__ float s_f[kSelWarps];
+  __shared__ int s_i[kSelWarps];
+  __shared__ int s_digit, s_cnt;
+  __shared__ unsigned long long s_above;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // Load, validate (finite and >= 0) and find the largest score.
+  float vmax = 0.f;
+  int bad = 0;
+  for (int i = tid; i < nb; i += blockDim.x) {
+    const float v = __ldcg(bs + i);
+    bad |= !(isfinite(v) && v >= 0.f);
+    sc.bits[i] = __float_as_uint(v);
+    vmax = fmaxf(vmax, v);
+    sc.keep[i] = 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    s_f[warp] = vmax;
+    s_i[warp] = bad;
+  }
+  __syncthreads();
+  vmax = 0.f;
+  bad = 0;
+  for (int w = 0; w < kSelWarps; ++w) {
+    vmax = fmaxf(vmax, s_f[w]);
+    bad |= s_i[w];
+  }
+  if (tid == 0) s_cnt = 0;
+  if (bad) {
+    if (tid == 0) set_status(status, UPF_ERR_NONFINITE);
+    for (int i = tid; i < nb; i += blockDim.x) sc.keep[i] = 1;
+  } else {
+    int ex = 0;
+    if (vmax > 0.f) frexpf(vmax, &ex);
+    const int sh = 48 - ex;
+    unsigned long long part = 0;
+    for (int i = tid; i < nb; i += blockDim.x) {
+      const unsigned long long m = vmax > 0.f ? fixed_mass(__uint_as_float(sc.bits[i]), sh) : 0ull;
+      sc.m[i] = m;
+      part += m;
+    }
+    const unsigned long long total = sel_block_sum(part, s_u64);
+    // Mass the selected prefix must reach: the smallest integer >= top_p * total.
+    const unsigned long long target = (unsigned long long)ceil((double)top_p * (double)total);
+    if (target > 0) {
+      uint32_t prefix = 0, pmask = 0;
+      unsigned long long above = 0;   // mass of blocks ranked strictly before the candidates
+      const int nb_pad = (nb + 31) & ~31;   // whole warps take part in the aggregation
+      for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int d = tid; d < 256; d += blockDim.x) h_mass[d] = 0;
+        __syncthreads();
+        for (int i = tid; i < nb_pad; i += blockDim.x) {
+          uint32_t digit = 256u + lane;        // nothing to add
+          unsigned long long m = 0;
+          if (i < nb) {
+            const uint32_t b = sc.bits[i];
+            if ((b & pmask) == prefix) {
+              digit = (b >> shift) & 255u;
+              m = sc.m[i];
+            }
+          }
+          hist_add_aggregated(h_mass, digit, m);
+        }
+        __syncthreads();
+        if (warp == 0) {
+          // Buckets from the highest digit down; lane l owns digits 255-8l .. 248-8l.
+          unsigned long long loc[8], lsum = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            loc[j] = h_mass[255 - 8 * lane - j];
+            lsum += loc[j];
+          }
+          unsigned long long incl = lsum;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+          }
+          const unsigned long long base = above + incl - lsum;   // mass before this lane's digits
+          const bool hit = base + lsum >= target && base < target;
+          const unsigned int who = __ballot_sync(0xffffffffu, hit);
+          const int src = who ? __ffs(who) - 1 : 31;
+          if (lane == src) {
+            unsigned long long run = base;
+            int dsel = 255 - 8 * lane - 7;
+            for (int j = 0; j < 8; ++j) {
+              if (run + loc[j] >= target) {
+                dsel = 255 - 8 * lane - j;
+                break;
+              }
+              run += loc[j];
+            }
+            s_digit = dsel;
+            s_above = run;
+          }
+        }
+        __syncthreads();
+        prefix |= uint32_t(s_digit) << shift;
+        pmask |= 255u << shift;
+        above = s_above;
+        __syncthreads();
+      }
+      // prefix = bits of the boundary score v*.  Blocks above it are in; the
+      // tied ones (equal scores) enter in index order until the mass suffices.
+      // Thread t owns the contiguous index range [t*per, (t+1)*per).
+      const int per = (nb + blockDim.x - 1) / blockDim.x;
+      const int i0 = min(nb, tid * per), i1 = min(nb, i0 + per);
+      int ties = 0;
+      unsigned long long w = 0;
+      for (int i = i0; i < i1; ++i) {
+        const uint32_t b = sc.bits[i];
+        if (b > prefix) sc.keep[i] = 1;
+        else if (b == prefix) {
+          ++ties;
+          w = sc.m[i];
+        }
+      }
+      // exclusive scan of tie counts in index order
+      int incl = ties;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (lane == 31) s_i[warp] = incl;
+      __syncthreads();
+      int before = incl - ties;
+      for (int ww = 0; ww < warp; ++ww) before += s_i[ww];
+      if (ties > 0) {
+        // every tied block carries the same mass w > 0 (the boundary bucket reached the target)
+        const unsigned long long need = target - above;
+        const unsigned long long take = w > 0 ? (need + w - 1) / w : 0;
+        int rank = before;
+        for (int i = i0; i < i1; ++i)
+          if (sc.bits[i] == prefix) {
+            if ((unsigned long long)rank < take) sc.keep[i] = 1;
+            ++rank;
+          }
+      }
+    }
+  }
+  __syncthreads();
+  // Exempt blocks: overlap with [0, sink) or [L - tail, L).
+  const int sink_hi = min(sink_keep, L);
+  const int tail_lo = max(0, L - tail_keep);
+  for (int i = tid; i < nb; i += blockDim.x) {
+    const int lo = i * G, hi = min(L, lo + G);
+    if (lo < sink_hi || hi > tail_lo) sc.keep[i] = 1;
+  }
+  __syncthreads();
+  // Kept tokens.
+  int cnt = 0;
+  for (int i = tid; i < nb; i += blockDim.x)
+    if (sc.keep[i]) cnt += min(L, (i + 1) * G) - i * G;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if (lane == 0 && cnt) atomicAdd(&s_cnt, cnt);
+  __syncthreads();
+  return s_cnt;
+}
+
+// Keep-bit word w of the packed tokens [tok0, tok0 + L) of a request whose
+// block flags are keep[]: bit (t % 32) set for kept tokens t of the request
+// in that word, 0 for tokens outside it.
+__device__ __forceinline__ uint32_t request_word_bits(const unsigned char* keep, int tok0, int L, int G, int w) {
+  uint32_t bits = 0;
+  const int t_lo = max(tok0, w * 32), t_hi = min(tok0 + L, w * 32 + 32);
+  for (int t = t_lo; t < t_hi;) {   // walk the blocks that overlap this word's tokens
+    const int blk = (t - tok0) / G;
+    const int t_end = min(t_hi, tok0 + (blk + 1) * G);
+    if (keep[blk]) {
+      const int len = t_end - t;
+      bits |= (len >= 32 ? 0xffffffffu : ((1u << len) - 1u)) << (t & 31);
+    }
+    t = t_end;
+  }
+  return bits;
+}
+
+}  // namespace upf

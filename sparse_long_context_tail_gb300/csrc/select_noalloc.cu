@@ -127,6 +127,8 @@ extern "C" upf_status upf_select_noalloc(const upf_batch* batch, const upf_param
   da.item_off2 = desc + (R + 1);
   da.blk_off = desc + 2 * (R + 1);
   da.status = status;
+  da.counters = nullptr;
+  da.ncounters = 0;
   cudaError_t e = upf::launch_describe(da, s);
   if (e != cudaSuccess) return reject(UPF_ERR_CUDA, "upf_select_noalloc: describe launch failed");
 

@@ -1,0 +1,343 @@
+// The tail of the per-layer path after scoring: finalize, block means,
+// top-p selection with exemption, the keep mask and the kept-token list, in
+// one launch; then the gather of the kept rows.
+//
+// UniPrefill article, section 二 second step (average the token scores inside
+// each block of G tokens, keep the smallest block set reaching p of the total
+// importance), the exemption paragraph (the first and last 128 tokens are
+// always kept), section 二 third step and section 三 (later layers see only
+// the kept tokens; positions, slot ids and the batch offsets follow the drop;
+// the decision stays on the GPU).
+//
+// tail_kernel: CTA c owns a run of consecutive blocks of the packed batch
+// (bpc blocks; a run may cross request boundaries).  Phase 1, every CTA: each
+// token's score (the sum of its per-group partials times 1/(H_q n_eff), or
+// the given score) and each block's mean.  Then each CTA counts itself done on
+// every request its run touches (one atomic per request); the CTA that
+// completes a request runs that request's selection (select_core.cuh) with all
+// its threads, writes the request's keep bits, its kept count and the packed
+// indices of its kept tokens (at the request's own offset in a list), and
+// counts the request done.  The CTA that completes the last request writes
+// the compacted batch offsets, the total, the keep-bit words shared by
+// neighbouring requests, and zero counts for empty requests.  Nothing waits:
+// completion is detected with fenced atomics, so there is no spin anywhere.
+//
+// The per-token and per-block sums follow the same order as the separate
+// finalize kernel (partials in index order, then tokens lane-strided within a
+// warp and a fixed shuffle tree), so the fused and the separate entry points
+// give the same bits.
+#include "select_core.cuh"
+#include "upf_internal.cuh"
+
+namespace upf {
+
+namespace {
+
+constexpr int kTailThreads = kSelThreads;   // 1024
+constexpr int kTailWarps = kTailThreads / 32;
+
+__device__ __forceinline__ int owner_of(const int32_t* off, int R, int x) {
+  int lo = 0, hi = R - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// The last request is done: offsets of the compacted batch, the total, the
+// keep-bit words shared by neighbouring requests (cleared, then the edge bits
+// of every request OR-ed in), and zero counts for empty requests.  Run by
+// the whole CTA.  With no blocks at all (an empty batch, or a descriptor the
+// describe kernel rejected), every count is 0 and every keep bit is cleared.
+__device__ void finish_batch(const TailArgs& a, bool no_blocks) {
+  __shared__ int s_carry;
+  __shared__ int s_warp[kTailWarps];
+  const SelectArgs& s = a.s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __threadfence();
+  if (no_blocks) {
+    const int nwords = (s.T + 31) / 32;
+    for (int w = tid; w < nwords; w += blockDim.x) s.keep_bits[w] = 0u;
+    for (int r = tid; r < s.R; r += blockDim.x) s.kept_count[r] = 0;
+  } else {
+    for (int r = tid; r < s.R; r += blockDim.x)
+      if (s.cu[r + 1] == s.cu[r]) s.kept_count[r] = 0;
+    // words a request covers only in part: clear, then OR in every request's part
+    for (int r = tid; r < s.R; r += blockDim.x) {
+      const int tok0 = s.cu[r], L = s.cu[r + 1] - tok0;
+      if (L <= 0) continue;
+      const int w0 = tok0 >> 5, w1 = (tok0 + L - 1) >> 5;
+      if (w0 * 32 < tok0 || w0 * 32 + 32 > tok0 + L) s.keep_bits[w0] = 0u;
+      if (w1 != w0 && w1 * 32 + 32 > tok0 + L) s.keep_bits[w1] = 0u;
+    }
+    __syncthreads();
+    for (int r = tid; r < s.R; r += blockDim.x) {
+      const int tok0 = s.cu[r], L = s.cu[r + 1] - tok0;
+      if (L <= 0) continue;
+      const int w0 = tok0 >> 5, w1 = (tok0 + L - 1) >> 5;
+      if (w0 * 32 < tok0 || w0 * 32 + 32 > tok0 + L) atomicOr(&s.keep_bits[w0], __ldcg(a.edge_bits + 2 * r));
+      if (w1 != w0 && w1 * 32 + 32 > tok0 + L) atomicOr(&s.keep_bits[w1], __ldcg(a.edge_bits + 2 * r + 1));
+    }
+  }
+  if (!a.cu_out) return;
+  // cu_out = exclusive prefix of the kept counts, in chunks of blockDim.x requests
+  if (tid == 0) s_carry = 0;
+  __syncthreads();
+  for (int base = 0; base < s.R; base += blockDim.x) {
+    const int r = base + tid;
+    const int v = (r < s.R && !no_blocks) ? __ldcg(s.kept_count + r) : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int before = s_carry;
+    for (int w = 0; w < warp; ++w) before += s_warp[w];
+    if (r < s.R) a.cu_out[r] = before + incl - v;
+    __syncthreads();
+    if (tid == blockDim.x - 1) s_carry = before + incl;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    a.cu_out[s.R] = s_carry;
+    *a.total_kept = s_carry;
+  }
+}
+
+// Selection of request r by the whole CTA, then its keep bits (whole words
+// inside the request by plain stores, the first and last word's bits to the
+// edge scratch), its count and its kept-token list.
+__device__ void select_and_emit(const TailArgs& a, int r, const SelectScratch& sc) {
+  __shared__ int s_warp[kTailWarps];
+  const SelectArgs& s = a.s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b0 = s.blk_off[r], nb = s.blk_off[r + 1] - b0;
+  const int tok0 = s.cu[r], L = s.cu[r + 1] - tok0;
+  __threadfence();
+  const int kept = select_request(s.block_scores + b0, nb, L, s.G, s.top_p, s.sink_keep, s.tail_keep, sc, s.status);
+  const int w0 = tok0 >> 5, w1 = (tok0 + L - 1) >> 5;
+  for (int w = w0 + tid; w <= w1; w += blockDim.x) {
+    const uint32_t bits = request_word_bits(sc.keep, tok0, L, s.G, w);
+    const bool partial = (w * 32 < tok0) || (w * 32 + 32 > tok0 + L);
+    if (!partial) s.keep_bits[w] = bits;
+    else if (w == w0) a.edge_bits[2 * r] = bits;
+    else a.edge_bits[2 * r + 1] = bits;
+  }
+  if (a.kept_list) {
+    // Output offset of every block (exclusive prefix of kept block sizes in
+    // block order), into sc.bits (free after the selection); thread t owns the
+    // contiguous blocks [t*per, (t+1)*per).
+    uint32_t* off = sc.bits;
+    const int per = (nb + blockDim.x - 1) / blockDim.x;
+    const int i0 = min(nb, tid * per), i1 = min(nb, i0 + per);
+    int mine = 0;
+    for (int i = i0; i < i1; ++i) mine += sc.keep[i] ? min(L, (i + 1) * s.G) - i * s.G : 0;
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int run = incl - mine;
+    for (int w = 0; w < warp; ++w) run += s_warp[w];
+    for (int i = i0; i < i1; ++i) {
+      off[i] = uint32_t(run);
+      run += sc.keep[i] ? min(L, (i + 1) * s.G) - i * s.G : 0;
+    }
+    __syncthreads();
+    // one warp per kept block: its tokens' packed indices, coalesced
+    for (int i = warp; i < nb; i += kTailWarps) {
+      if (!sc.keep[i]) continue;
+      const int lo = i * s.G, n = min(L, lo + s.G) - lo;
+      int32_t* dst = a.kept_list + tok0 + off[i];
+      for (int j = lane; j < n; j += 32) dst[j] = tok0 + lo + j;
+    }
+  }
+  if (tid == 0) s.kept_count[r] = kept;
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ unsigned char s_dyn[];
+  __shared__ int s_bstart[kTailMaxBpc + 1];   // first packed token of each owned block, then the run's end
+  __shared__ float s_inv[kTailMaxBpc];
+  __shared__ int s_sel[kTailMaxBpc];
+  __shared__ int s_nsel, s_last;
+  const SelectArgs& s = a.s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nb_total = s.blk_off[s.R];   // 0 if the describe kernel rejected the descriptor
+  if (nb_total == 0) {
+    if (blockIdx.x == 0) finish_batch(a, true);
+    return;
+  }
+  const int b0 = blockIdx.x * a.bpc;
+  if (b0 >= nb_total) return;
+  const int b1 = min(nb_total, b0 + a.bpc);
+  const int nown = b1 - b0;
+  // Token ranges of the owned blocks (consecutive blocks are consecutive
+  // tokens of the packed batch) and each block's 1/(H_q n_eff).
+  if (tid <= nown) {
+    const int b = b0 + min(tid, nown - 1);
+    const int r = owner_of(s.blk_off, s.R, b);
+    const int i = b - s.blk_off[r];
+    const int tok0 = s.cu[r], L = s.cu[r + 1] - tok0;
+    if (tid < nown) {
+      s_bstart[tid] = tok0 + i * s.G;
+      s_inv[tid] = 1.0f / float(s.Hq * min(s.n, L));
+    } else {
+      s_bstart[nown] = tok0 + min(L, (i + 1) * s.G);
+    }
+  }
+  if (tid == 0) {
+    s_nsel = 0;
+    s_last = 0;
+  }
+  __syncthreads();
+  const int tfirst = s_bstart[0], ntok = s_bstart[nown] - tfirst;
+  float* s_val = reinterpret_cast<float*>(s_dyn);   // [ntok] token scores of the run
+  for (int j = tid; j < ntok; j += blockDim.x) {
+    const int t = tfirst + j;
+    float v;
+    if (s.P > 0) {
+      int k = 0, hi = nown - 1;   // owned block of token t: the last k with s_bstart[k] <= t
+      while (k < hi) {
+        const int mid = (k + hi + 1) >> 1;
+        if (s_bstart[mid] <= t) k = mid;
+        else hi = mid - 1;
+      }
+      v = 0.f;
+#pragma unroll 8
+      for (int c = 0; c < s.P; ++c) v += s.part[(int64_t)c * s.T + t];
+      v *= s_inv[k];
+      if (s.scores_out) s.scores_out[t] = v;
+    } else {
+      v = s.scores_in[t];
+    }
+    s_val[j] = v;
+  }
+  __syncthreads();
+  for (int k = warp; k < nown; k += kTailWarps) {
+    const int lo = s_bstart[k] - tfirst, hi = s_bstart[k + 1] - tfirst;
+    float sum = 0.f;
+    for (int j = lo + lane; j < hi; j += 32) sum += s_val[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) s.block_scores[b0 + k] = sum / float(hi - lo);
+  }
+  // Every writer fences, then one thread publishes with the atomics.
+  __threadfence();
+  __syncthreads();
+  // Count this CTA done on every request its run touches; keep the ones it completes.
+  if (tid == 0) {
+    const int r_first = owner_of(s.blk_off, s.R, b0), r_last = owner_of(s.blk_off, s.R, b1 - 1);
+    int nsel = 0;
+    for (int r = r_first; r <= r_last; ++r) {
+      const int f = s.blk_off[r], e = s.blk_off[r + 1];
+      if (e == f) continue;   // empty request (no blocks)
+      const int ctas = (e - 1) / a.bpc - f / a.bpc + 1;
+      if (atomicAdd(a.counters + r, 1) == ctas - 1) s_sel[nsel++] = r;
+    }
+    s_nsel = nsel;
+  }
+  __syncthreads();
+  const int nsel = s_nsel;
+  if (nsel == 0) return;
+  const SelectScratch sc = carve_select(s_dyn, a.nbp);
+  for (int k = 0; k < nsel; ++k) select_and_emit(a, s_sel[k], sc);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    if (atomicAdd(a.counters + s.R, nsel) + nsel == a.nonempty) s_last = 1;
+  }
+  __syncthreads();
+  if (s_last) finish_batch(a, false);
+}
+
+// The gather of the fused path: output row o belongs to the request r with
+// cu_out[r] <= o < cu_out[r+1]; its input row is entry o - cu_out[r] of r's
+// kept-token list.  One warp per output row, 16-byte vectors, eight in
+// flight per lane; block 0 appends the drop-history record.
+__global__ void __launch_bounds__(256) gather_list_kernel(const CompactArgs a, const int32_t* kept_list) {
+  pdl_trigger();
+  pdl_wait();
+  const int total = min(*a.total_kept, a.T);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && a.history) {
+    bool full = false;
+    for (int r = 0; r < a.R; ++r) full |= a.history_len[r] >= a.history_cap || a.history_len[r] < 0;
+    if (full) {
+      set_status(a.status, UPF_ERR_CAPACITY);
+    } else {
+      for (int r = 0; r < a.R; ++r) {
+        const int len = a.history_len[r];
+        int32_t* rec = a.history + ((int64_t)r * a.history_cap + len) * 2;
+        rec[0] = a.layer_id;
+        rec[1] = a.cu_out[r + 1] - a.cu_out[r];
+        a.history_len[r] = len + 1;
+      }
+    }
+  }
+  const int lane = threadIdx.x & 31;
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  const int64_t nvec = a.row_bytes / 16;
+  for (int o = warp; o < total; o += nwarps) {
+    const int r = owner_of(a.cu_out, a.R, o);
+    const int t = kept_list[a.cu[r] + (o - a.cu_out[r])];
+    if (t < 0 || t >= a.T) continue;   // never for a consistent batch; no access outside the buffers
+    if (lane == 0 && a.kept_index) a.kept_index[o] = t;
+    if (a.hidden_in) {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(a.hidden_in) + (int64_t)t * a.row_bytes);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(a.hidden_out) + (int64_t)o * a.row_bytes);
+      int64_t v = lane;
+      for (; v + 224 < nvec; v += 256) {
+        uint4 x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = __ldcs(src + v + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) __stcs(dst + v + 32 * u, x[u]);
+      }
+      for (; v < nvec; v += 32) __stcs(dst + v, __ldcs(src + v));
+    }
+    if (lane == 1 && a.pos_in) a.pos_out[o] = a.pos_in[t];
+    if (lane == 2 && a.slot_in) a.slot_out[o] = a.slot_in[t];
+  }
+}
+
+}  // namespace
+
+int tail_blocks_per_cta(int G) {
+  int bpc = G > 0 ? 2048 / G : 1;
+  return bpc < 1 ? 1 : (bpc > kTailMaxBpc ? kTailMaxBpc : bpc);
+}
+
+size_t tail_smem_bytes(int G, int max_nb) {
+  const int nbp = ((max_nb > 0 ? max_nb : 1) + 7) & ~7;
+  const size_t sel = select_smem_bytes(nbp);
+  const size_t vals = sizeof(float) * size_t(tail_blocks_per_cta(G)) * size_t(G);
+  return sel > vals ? sel : vals;
+}
+
+cudaError_t launch_tail(const TailArgs& a, cudaStream_t s, bool pdl) {
+  const size_t smem = tail_smem_bytes(a.s.G, a.s.max_nb);
+  cudaError_t e = cudaFuncSetAttribute(tail_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  const int grid = a.s.NB > 0 ? (a.s.NB + a.bpc - 1) / a.bpc : 1;
+  return launch_kernel(tail_kernel, grid, kTailThreads, smem, s, pdl, a);
+}
+
+cudaError_t launch_gather_list(const CompactArgs& a, const int32_t* kept_list, cudaStream_t s, bool pdl) {
+  int blocks = (a.T + 7) / 8;
+  blocks = blocks < 1 ? 1 : (blocks > 8 * kPlanSMs ? 8 * kPlanSMs : blocks);
+  return launch_kernel(gather_list_kernel, blocks, 256, 0, s, pdl, a, kept_list);
+}
+
+}  // namespace upf

@@ -4,6 +4,7 @@
 // Nothing here allocates except upf_create (one small device status word).
 // Every launch goes to the caller's stream; argument errors are reported before
 // the first launch.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -90,8 +91,13 @@ struct Plan {
   int nwords = 0, nchunks = 0;
   std::vector<int32_t> qhead;
   // workspace offsets
-  size_t off_desc = 0, off_p1 = 0, off_part = 0, off_bs = 0, off_chunk = 0, off_kidx = 0, total = 0;
+  size_t off_desc = 0, off_p1 = 0, off_part = 0, off_bs = 0, off_chunk = 0, off_kidx = 0, off_ctr = 0, total = 0;
+  int nonempty = 0;
 };
+
+// The fused tail kernel serves blocks up to kTailMaxBlock tokens; larger
+// blocks take the separate finalize, select and compaction kernels.
+bool fused_tail(const Plan& pl) { return pl.G >= 1 && pl.G <= upf::kTailMaxBlock; }
 
 upf_status check_batch(const upf_batch* b) {
   if (!b) return fail(UPF_ERR_INVALID_ARG, "batch is NULL");
@@ -143,7 +149,7 @@ upf_status check_params(const upf_params* p) {
 int ceil_div(long long a, long long b) { return int((a + b - 1) / b); }
 
 // Keys per split so that the pass has about `target` items in total: a
-// multiple of `tile` keys, at least 256.
+// multiple of `tile` keys, at least 256 (the CUDA-core kernels, a few waves).
 int choose_split(const upf_batch* b, int per_req_units, long long target, int tile) {
   long long keys = 0;
   for (int r = 0; r < b->num_reqs; ++r) keys += b->cu_seqlens_host[r + 1] - b->cu_seqlens_host[r];
@@ -152,6 +158,105 @@ int choose_split(const upf_batch* b, int per_req_units, long long target, int ti
   ks = ((ks + tile - 1) / tile) * tile;
   if (ks < 256) ks = 256;
   return int(std::min<long long>(ks, 1 << 30));
+}
+
+long long split_items(const upf_batch* b, int units, long long ks) {
+  long long n = 0;
+  for (int r = 0; r < b->num_reqs; ++r) n += (long long)units * ceil_div(b->cu_seqlens_host[r + 1] - b->cu_seqlens_host[r], ks);
+  return n;
+}
+
+// Estimated duration of a tensor-core pass with key splits of ks keys: the
+// items, in launch order (request, kv head, split, query chunk), go to the
+// first SM that is free (one CTA per SM); an item costs its keys plus a
+// fixed start-up of `ovh` keys (query chunk load, tensor memory, pipeline
+// fill and drain).
+long long split_makespan(const upf_batch* b, int hkv, int nqc, long long ks, long long ovh, int sms) {
+  std::vector<long long> heap(size_t(sms), 0);   // min-heap of SM finish times
+  auto push_pop = [&](long long cost) {
+    long long t = heap[0] + cost;
+    size_t i = 0;   // replace the root and sift down
+    for (;;) {
+      size_t l = 2 * i + 1, r = l + 1, m = i;
+      long long tm = t;
+      if (l < heap.size() && heap[l] < tm) { m = l; tm = heap[l]; }
+      if (r < heap.size() && heap[r] < tm) { m = r; tm = heap[r]; }
+      if (m == i) break;
+      heap[i] = heap[m];
+      i = m;
+    }
+    heap[i] = t;
+  };
+  for (int r = 0; r < b->num_reqs; ++r) {
+    const long long L = b->cu_seqlens_host[r + 1] - b->cu_seqlens_host[r];
+    const long long nsplit = (L + ks - 1) / ks;
+    for (int g = 0; g < hkv; ++g)
+      for (long long sp = 0; sp < nsplit; ++sp)
+        for (int qc = 0; qc < nqc; ++qc) push_pop(std::min(ks, L - sp * ks) + ovh);
+  }
+  return *std::max_element(heap.begin(), heap.end());
+}
+
+// Key splits of the tensor-core passes (one CTA per SM, one item per CTA).
+// Rounding the ideal split up to whole tiles can leave a few items over a
+// whole wave (160 items on 152 SMs take two item-times), so the split is
+// chosen among the smallest splits that fit the items into 1..4 waves, by
+// the estimated duration of each.
+int choose_split_tc(const upf_batch* b, int hkv, int nqc, int tile, int sms) {
+  const int units = hkv * nqc;
+  long long keys = 0, max_len = 0;
+  for (int r = 0; r < b->num_reqs; ++r) {
+    const long long L = b->cu_seqlens_host[r + 1] - b->cu_seqlens_host[r];
+    keys += L;
+    max_len = std::max(max_len, L);
+  }
+  auto round_tile = [&](long long x) { return std::max<long long>(256, ((x + tile - 1) / tile) * tile); };
+  const long long hi_ks = round_tile(std::max<long long>(max_len, 1));
+  long long best = round_tile((keys * units + sms - 1) / sms);
+  if (best > hi_ks) best = hi_ks;
+  const long long n_best = split_items(b, units, best);
+  // One wave already: no smaller split fits one wave, and more waves only add start-ups.
+  if (n_best <= sms || n_best > (1LL << 20)) return int(std::min<long long>(best, 1 << 30));
+  // The simulation below costs host time; batches repeat across layers and steps.
+  struct Entry {
+    uint64_t key = 0;
+    int ks = 0;
+  };
+  thread_local Entry cache[8];
+  thread_local int cache_next = 0;
+  uint64_t key = 1469598103934665603ULL;
+  auto mix = [&](uint64_t v) { key = (key ^ v) * 1099511628211ULL; };
+  mix(uint64_t(b->num_reqs));
+  mix(uint64_t(hkv));
+  mix(uint64_t(nqc));
+  mix(uint64_t(tile));
+  mix(uint64_t(sms));
+  for (int r = 0; r <= b->num_reqs; ++r) mix(uint64_t(uint32_t(b->cu_seqlens_host[r])));
+  for (const Entry& e : cache)
+    if (e.ks && e.key == key) return e.ks;
+  const long long ovh = 2LL * tile;
+  long long best_t = split_makespan(b, hkv, nqc, best, ovh, sms);
+  for (int w = 1; w <= 4; ++w) {
+    // smallest whole-tile split with at most w * sms items (items fall as the split grows)
+    long long lo = round_tile((keys * units + (long long)w * sms - 1) / ((long long)w * sms)), hi = hi_ks;
+    if (lo > hi) lo = hi;
+    while (lo < hi) {
+      const long long mid = round_tile(lo + (hi - lo) / 2);
+      if (mid >= hi) break;
+      if (split_items(b, units, mid) <= (long long)w * sms) hi = mid;
+      else lo = mid + tile;
+    }
+    const long long ks = split_items(b, units, lo) <= (long long)w * sms ? lo : hi;
+    const long long t = split_makespan(b, hkv, nqc, ks, ovh, sms);
+    if (t < best_t || (t == best_t && ks > best)) {
+      best_t = t;
+      best = ks;
+    }
+  }
+  const int chosen = int(std::min<long long>(best, 1 << 30));
+  cache[cache_next] = Entry{key, chosen};
+  cache_next = (cache_next + 1) % 8;
+  return chosen;
 }
 
 upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p, bool need_heads, Plan* pl) {
@@ -197,11 +302,13 @@ upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p
     // depends only on the batch and parameters (never on the device), so
     // upf_workspace_bytes() without a context sizes exactly what a call uses.
     (void)ctx;
-    const long long target = (pl->use_tc ? 1LL : 4LL) * upf::kPlanSMs;
-    const int tile1 = pl->use_tc ? upf::score_tc_key_tile(1, pl->d) : 128;
-    const int tile2 = pl->use_tc ? upf::score_tc_key_tile(2, pl->d) : 128;
-    pl->KS1 = choose_split(b, pl->Hkv * pl->NQC, target, tile1);
-    pl->KS2 = choose_split(b, pl->Hkv * pl->NQC, target, tile2);
+    if (pl->use_tc) {
+      pl->KS1 = choose_split_tc(b, pl->Hkv, pl->NQC, upf::score_tc_key_tile(1, pl->d), upf::kPlanSMs);
+      pl->KS2 = choose_split_tc(b, pl->Hkv, pl->NQC, upf::score_tc_key_tile(2, pl->d), upf::kPlanSMs);
+    } else {
+      pl->KS1 = choose_split(b, pl->Hkv * pl->NQC, 4LL * upf::kPlanSMs, 128);
+      pl->KS2 = choose_split(b, pl->Hkv * pl->NQC, 4LL * upf::kPlanSMs, 128);
+    }
     pl->pw = pl->use_tc ? upf::kTcPartials : 1;
     pl->items1 = pl->items2 = 0;
     pl->NB = 0;
@@ -240,7 +347,11 @@ upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p
   off = align256(off + sizeof(int32_t) * pl->nchunks);
   pl->off_kidx = off;
   off = align256(off + sizeof(int32_t) * size_t(pl->T));
+  pl->off_ctr = off;   // tail counters [R+1], then edge words [2R]
+  off = align256(off + sizeof(int32_t) * size_t(pl->R + 1) + sizeof(uint32_t) * 2 * size_t(pl->R));
   pl->total = off;
+  pl->nonempty = 0;
+  for (int r = 0; r < pl->R; ++r) pl->nonempty += b->cu_seqlens_host[r + 1] > b->cu_seqlens_host[r];
   return UPF_OK;
 }
 
@@ -372,7 +483,25 @@ upf::DescribeArgs describe_args(const upf_ctx* ctx, const upf_batch* b, const Pl
   a.item_off2 = a.item_off1 + (pl.R + 1);
   a.blk_off = a.item_off2 + (pl.R + 1);
   a.status = ctx->status_dev;
+  a.counters = at<int32_t>(ws, pl.off_ctr);
+  a.ncounters = pl.R + 1;
   return a;
+}
+
+// Arguments of the fused tail; kept_list / cu_out / total_kept nullable.
+upf::TailArgs tail_args(const upf::SelectArgs& se, const Plan& pl, void* ws, int32_t* kept_list, int32_t* cu_out,
+                        int32_t* total_kept) {
+  upf::TailArgs t;
+  t.s = se;
+  t.counters = at<int32_t>(ws, pl.off_ctr);
+  t.edge_bits = reinterpret_cast<uint32_t*>(t.counters + (pl.R + 1));
+  t.kept_list = kept_list;
+  t.cu_out = cu_out;
+  t.total_kept = total_kept;
+  t.nonempty = pl.nonempty;
+  t.bpc = upf::tail_blocks_per_cta(pl.G);
+  t.nbp = ((pl.max_nb > 0 ? pl.max_nb : 1) + 7) & ~7;
+  return t;
 }
 
 upf::SelectArgs select_args(const upf_ctx* ctx, const upf_batch* b, const Plan& pl, void* ws, int P,
@@ -637,6 +766,18 @@ static upf_status score_impl(upf_ctx* ctx, const upf_batch* batch, const upf_par
   return UPF_OK;
 }
 
+upf_status upf_plan_info(const upf_batch* batch, const upf_params* params, int32_t* key_split1, int32_t* key_split2,
+                         int64_t* items1, int64_t* items2) {
+  Plan pl;
+  upf_status st = make_plan(nullptr, batch, params, true, &pl);
+  if (st != UPF_OK) return st;
+  if (key_split1) *key_split1 = pl.KS1;
+  if (key_split2) *key_split2 = pl.KS2;
+  if (items1) *items1 = pl.items1;
+  if (items2) *items2 = pl.items2;
+  return UPF_OK;
+}
+
 upf_status upf_score(upf_ctx* ctx, const upf_batch* batch, const upf_params* params, const void* q,
                      int64_t q_row_stride, const void* k, int64_t k_row_stride, float* scores, void* ws,
                      size_t ws_bytes, void* stream) {
@@ -675,6 +816,11 @@ upf_status upf_select(upf_ctx* ctx, const upf_batch* batch, const upf_params* pa
   UPF_LAUNCH(staged(ctx, kDescribe, s, [&] { return upf::launch_describe(da, s, false); }), "describe");
   upf::SelectArgs se = select_args(ctx, batch, pl, ws, 0, nullptr, scores, nullptr, block_scores, keep_bits,
                                    kept_count);
+  if (fused_tail(pl)) {
+    const upf::TailArgs ta = tail_args(se, pl, ws, nullptr, nullptr, nullptr);
+    UPF_LAUNCH(staged(ctx, kSelect, s, [&] { return upf::launch_tail(ta, s, true); }), "block means and select");
+    return UPF_OK;
+  }
   UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s, true); }), "block means");
   UPF_LAUNCH(staged(ctx, kSelect, s, [&] { return upf::launch_select(se, s, true); }), "select");
   return UPF_OK;
@@ -691,7 +837,6 @@ upf_status upf_compact(upf_ctx* ctx, const upf_batch* batch, const uint32_t* kee
   DeviceGuard guard(ctx->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return launch_compact_all(ctx, compact_args(ctx, batch, pl, keep_bits, io, ws), s, false);
-  return UPF_OK;
 }
 
 upf_status upf_revive(upf_ctx* ctx, const upf_batch* batch, const int32_t* kept_index, const int32_t* total_kept,
@@ -756,10 +901,21 @@ upf_status upf_select_tokens(upf_ctx* ctx, const upf_batch* batch, const upf_par
   UPF_LAUNCH(staged(ctx, kPass2, s, [&] { return upf::launch_score_pass2(sa, s, true); }), "score pass 2");
   upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC * pl.pw, sa.part, nullptr, scores, block_scores,
                                    keep_bits, kept_count);
+  if (fused_tail(pl)) {
+    // finalize + block means + select + kept-token list + compacted offsets in
+    // one launch, then the gather driven by the per-request lists
+    int32_t* kept_list = at<int32_t>(ws, pl.off_kidx);
+    const upf::TailArgs ta = tail_args(se, pl, ws, kept_list, io->cu_seqlens_out, io->total_kept);
+    UPF_LAUNCH(staged(ctx, kSelect, s, [&] { return upf::launch_tail(ta, s, true); }), "finalize and select");
+    upf::CompactArgs ca = compact_args(ctx, batch, pl, keep_bits, io, ws);
+    ca.kept_index = io->kept_index;   // the workspace's index area holds the lists
+    UPF_LAUNCH(staged(ctx, kCompactGather, s, [&] { return upf::launch_gather_list(ca, kept_list, s, true); }),
+               "compact gather");
+    return UPF_OK;
+  }
   UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s, true); }), "finalize scores");
   UPF_LAUNCH(staged(ctx, kSelect, s, [&] { return upf::launch_select(se, s, true); }), "select");
   return launch_compact_all(ctx, compact_args(ctx, batch, pl, keep_bits, io, ws), s, true);
-  return UPF_OK;
 }
 
 }  // extern "C"

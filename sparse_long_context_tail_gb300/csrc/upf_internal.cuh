@@ -66,6 +66,8 @@ struct DescribeArgs {
   int32_t* item_off2;
   int32_t* blk_off;
   int32_t* status;
+  int32_t* counters;     // [ncounters] cleared here for the tail kernel (nullable)
+  int32_t ncounters;
 };
 
 struct SelectArgs {
@@ -84,6 +86,23 @@ struct SelectArgs {
   uint32_t* keep_bits;    // [ceil(T/32)]
   int32_t* kept_count;    // [R]
   int32_t* status;
+};
+
+// The fused tail (finalize, block means, selection, keep bits, kept-token
+// list, compacted offsets) of upf_select_tokens and upf_select.
+constexpr int kTailMaxBpc = 32;   // blocks per CTA of the tail kernel (upper bound)
+constexpr int kTailMaxBlock = 4096;  // larger G take the separate kernels
+
+struct TailArgs {
+  SelectArgs s;
+  int32_t* counters;    // [R+1], zero on entry: CTAs done per request, then requests done
+  uint32_t* edge_bits;  // [2R] keep bits of each request's first and last word when shared
+  int32_t* kept_list;   // [T] (nullable): request r's kept tokens at [cu[r], cu[r] + kept_r)
+  int32_t* cu_out;      // [R+1] (nullable, then total_kept too)
+  int32_t* total_kept;  // [1]
+  int32_t nonempty;     // requests with at least one token (host value)
+  int32_t bpc;          // blocks per CTA
+  int32_t nbp;          // selection scratch capacity in blocks (multiple of 8, >= max_nb)
 };
 
 struct CompactArgs {
@@ -171,6 +190,10 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t s, bool pdl = false)
 cudaError_t launch_compact_count(const CompactArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_compact_index(const CompactArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_compact_gather(const CompactArgs& a, cudaStream_t s, bool pdl = false);
+int tail_blocks_per_cta(int G);
+size_t tail_smem_bytes(int G, int max_nb);
+cudaError_t launch_tail(const TailArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_gather_list(const CompactArgs& a, const int32_t* kept_list, cudaStream_t s, bool pdl = false);
 cudaError_t launch_revive(const ReviveArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_history_kv_len(const HistoryArgs& a, cudaStream_t s, bool pdl = false);
 

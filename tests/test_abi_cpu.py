@@ -103,3 +103,22 @@ def test_wait_limit_and_shard_scoring_check_their_arguments(lib):
     with pytest.raises(B.UpfError) as e:
         B.upf_score_shard(None, b, B.make_params(), 32, 16, 4096, 16, 1024, 16, 256, 1 << 20)
     assert e.value.status == 1
+
+
+def test_scoring_work_split_fills_whole_waves_on_every_benchmark_workload(lib):
+    """The tensor-core passes run one CTA per SM (152 on GB300): a single-request
+    batch must not leave a few items over a whole wave (160 items on 152 SMs
+    take two item-times), and splits stay whole key tiles."""
+    from sparse_long_context_tail_gb300 import workload as wl
+    for name in wl.NAMED:
+        s = wl.named_spec(name)
+        cu = np.concatenate([[0], np.cumsum(s.lengths)]).astype(np.int32)
+        b, keep = B.make_batch(0x1000, cu, s.num_q_heads, s.num_kv_heads, s.head_dim)
+        p = B.make_params(s.n_tail, s.block, s.sink_keep, s.tail_keep, s.top_p)
+        ks1, ks2, n1, n2 = B.upf_plan_info(b, p)
+        tile1 = 256 if s.head_dim <= 128 else 128
+        assert ks1 % tile1 == 0 and ks2 % 128 == 0 and min(ks1, ks2) >= 256, name
+        for n in (n1, n2):
+            assert 0 < n <= 4 * 152, (name, n)
+            if len(s.lengths) == 1:
+                assert n <= 152 or n % 152 == 0, (name, n)
