@@ -291,8 +291,10 @@ __global__ void __launch_bounds__(256) gather_list_kernel(const CompactArgs a, c
   const int64_t nvec = a.row_bytes / 16;
   for (int o = warp; o < total; o += nwarps) {
     const int r = owner_of(a.cu_out, a.R, o);
-    const int t = kept_list[a.cu[r] + (o - a.cu_out[r])];
-    if (t < 0 || t >= a.T) continue;   // never for a consistent batch; no access outside the buffers
+    const int at = a.cu[r] + (o - a.cu_out[r]);
+    if (at < 0 || at >= a.T) continue;   // never for a consistent batch; no access outside the buffers
+    const int t = kept_list[at];
+    if (t < 0 || t >= a.T) continue;
     if (lane == 0 && a.kept_index) a.kept_index[o] = t;
     if (a.hidden_in) {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(a.hidden_in) + (int64_t)t * a.row_bytes);
