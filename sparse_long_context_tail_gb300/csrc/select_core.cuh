@@ -76,17 +76,28 @@ __device__ __forceinline__ T sel_block_sum(T v, T* s_tmp) {
   return t;
 }
 
-// Adds `mass` to hist[digit] for every lane with digit < 256, one shared
-// atomic per distinct digit of the warp.  Every lane of the warp must call it
-// (lanes with nothing to add pass digit >= 256 and a distinct value each).
+// Adds `mass` to hist[digit] for every lane with digit < 256.  Every lane of
+// the warp calls it (lanes with nothing to add pass digit >= 256).  Up to four
+// times, the lanes sharing the digit of the lowest lane still pending add
+// their masses with two full-warp reductions of 24-bit halves (no sum
+// overflows 32 bits) and one lane does a single shared atomic; lanes left
+// after that (digits already spread out) add their own.
 __device__ __forceinline__ void hist_add_aggregated(unsigned long long* hist, uint32_t digit,
                                                     unsigned long long mass) {
-  const unsigned peers = __match_any_sync(0xffffffffu, digit);
-  const uint32_t lo = __reduce_add_sync(peers, uint32_t(mass & 0xFFFFFFull));
-  const uint32_t hi = __reduce_add_sync(peers, uint32_t(mass >> 24));
   const int lane = threadIdx.x & 31;
-  if (digit < 256u && lane == __ffs(peers) - 1)
-    atomicAdd(&hist[digit], (unsigned long long)lo + ((unsigned long long)hi << 24));
+  unsigned pending = __ballot_sync(0xffffffffu, digit < 256u);
+#pragma unroll 1
+  for (int it = 0; it < 4 && pending; ++it) {
+    const int leader = __ffs(pending) - 1;
+    const uint32_t d = __shfl_sync(0xffffffffu, digit, leader);
+    const bool mine = ((pending >> lane) & 1u) && digit == d;
+    const unsigned group = __ballot_sync(0xffffffffu, mine);
+    const uint32_t lo = __reduce_add_sync(0xffffffffu, mine ? uint32_t(mass & 0xFFFFFFull) : 0u);
+    const uint32_t hi = __reduce_add_sync(0xffffffffu, mine ? uint32_t(mass >> 24) : 0u);
+    if (lane == leader) atomicAdd(&hist[d], (unsigned long long)lo + ((unsigned long long)hi << 24));
+    pending &= ~group;
+  }
+  if ((pending >> lane) & 1u) atomicAdd(&hist[digit], mass);
 }
 
 // Selects the blocks of one request: block scores bs[0..nb) (global, any
@@ -96,7 +107,7 @@ __device__ __forceinline__ void hist_add_aggregated(unsigned long long* hist, ui
 // score keeps the whole request and records UPF_ERR_NONFINITE.
 static __device__ int select_request(const float* bs, int nb, int L, int G, float top_p, int sink_keep, int tail_keep,
                               const SelectScratch& sc, int32_t* status) {
-  __shared__ unsigned long long h_mass[256];
+  __shared__ unsigned long long h_mass[2][256];   // this round's histogram and the next one's, cleared meanwhile
   __shared__ unsigned long long s_u64[kSelWarps];
   __shared__ float s_f[kSelWarps];
   __shared__ int s_i[kSelWarps];
@@ -141,6 +152,7 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
       sc.m[i] = m;
       part += m;
     }
+    for (int d = tid; d < 256; d += blockDim.x) h_mass[0][d] = 0;   // ordered by the barriers in the sum
     const unsigned long long total = sel_block_sum(part, s_u64);
     // Mass the selected prefix must reach: the smallest integer >= top_p * total.
     const unsigned long long target = (unsigned long long)ceil((double)top_p * (double)total);
@@ -148,9 +160,9 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
       uint32_t prefix = 0, pmask = 0;
       unsigned long long above = 0;   // mass of blocks ranked strictly before the candidates
       const int nb_pad = (nb + 31) & ~31;   // whole warps take part in the aggregation
-      for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int d = tid; d < 256; d += blockDim.x) h_mass[d] = 0;
-        __syncthreads();
+      int cur = 0;
+      for (int shift = 24; shift >= 0; shift -= 8, cur ^= 1) {
+        unsigned long long* hist = h_mass[cur];
         for (int i = tid; i < nb_pad; i += blockDim.x) {
           uint32_t digit = 256u + lane;        // nothing to add
           unsigned long long m = 0;
@@ -161,7 +173,7 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
               m = sc.m[i];
             }
           }
-          hist_add_aggregated(h_mass, digit, m);
+          hist_add_aggregated(hist, digit, m);
         }
         __syncthreads();
         if (warp == 0) {
@@ -169,7 +181,7 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
           unsigned long long loc[8], lsum = 0;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            loc[j] = h_mass[255 - 8 * lane - j];
+            loc[j] = hist[255 - 8 * lane - j];
             lsum += loc[j];
           }
           unsigned long long incl = lsum;
@@ -195,12 +207,15 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
             s_digit = dsel;
             s_above = run;
           }
+        } else if (tid < 32 + 256) {
+          h_mass[cur ^ 1][tid - 32] = 0;   // the next round's histogram
         }
         __syncthreads();
         prefix |= uint32_t(s_digit) << shift;
         pmask |= 255u << shift;
         above = s_above;
-        __syncthreads();
+        // s_digit / s_above are rewritten only after the next round's first
+        // barrier, which every thread reaches after reading them here.
       }
       // prefix = bits of the boundary score v*.  Blocks above it are in; the
       // tied ones (equal scores) enter in index order until the mass suffices.

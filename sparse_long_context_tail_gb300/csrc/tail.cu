@@ -36,6 +36,16 @@ namespace {
 constexpr int kTailThreads = kSelThreads;   // 1024
 constexpr int kTailWarps = kTailThreads / 32;
 
+// Counter increment with acquire-release semantics at GPU scope: it publishes
+// what this CTA wrote before the preceding barrier and, when it returns the
+// final count, makes the other CTAs' published writes visible to this CTA
+// (after the next barrier).
+__device__ __forceinline__ int add_acq_rel(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ int owner_of(const int32_t* off, int R, int x) {
   int lo = 0, hi = R - 1;
   while (lo < hi) {
@@ -56,7 +66,6 @@ __device__ void finish_batch(const TailArgs& a, bool no_blocks) {
   __shared__ int s_warp[kTailWarps];
   const SelectArgs& s = a.s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __threadfence();
   if (no_blocks) {
     const int nwords = (s.T + 31) / 32;
     for (int w = tid; w < nwords; w += blockDim.x) s.keep_bits[w] = 0u;
@@ -118,15 +127,16 @@ __device__ void select_and_emit(const TailArgs& a, int r, const SelectScratch& s
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b0 = s.blk_off[r], nb = s.blk_off[r + 1] - b0;
   const int tok0 = s.cu[r], L = s.cu[r + 1] - tok0;
-  __threadfence();
   const int kept = select_request(s.block_scores + b0, nb, L, s.G, s.top_p, s.sink_keep, s.tail_keep, sc, s.status);
   const int w0 = tok0 >> 5, w1 = (tok0 + L - 1) >> 5;
   for (int w = w0 + tid; w <= w1; w += blockDim.x) {
     const uint32_t bits = request_word_bits(sc.keep, tok0, L, s.G, w);
     const bool partial = (w * 32 < tok0) || (w * 32 + 32 > tok0 + L);
-    if (!partial) s.keep_bits[w] = bits;
-    else if (w == w0) a.edge_bits[2 * r] = bits;
-    else a.edge_bits[2 * r + 1] = bits;
+    if (!partial) {
+      s.keep_bits[w] = bits;
+    } else {   // read by the CTA that finishes the batch
+      a.edge_bits[2 * r + (w == w0 ? 0 : 1)] = bits;
+    }
   }
   if (a.kept_list) {
     // Output offset of every block (exclusive prefix of kept block sizes in
@@ -160,7 +170,7 @@ __device__ void select_and_emit(const TailArgs& a, int r, const SelectScratch& s
       for (int j = lane; j < n; j += 32) dst[j] = tok0 + lo + j;
     }
   }
-  if (tid == 0) s.kept_count[r] = kept;
+  if (tid == 0) s.kept_count[r] = kept;   // read by the CTA that finishes the batch
   __syncthreads();
 }
 
@@ -231,12 +241,12 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailArgs a) {
     for (int j = lo + lane; j < hi; j += 32) sum += s_val[j];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) s.block_scores[b0 + k] = sum / float(hi - lo);
+    if (lane == 0) s.block_scores[b0 + k] = sum / float(hi - lo);   // read by the selecting CTA
   }
-  // Every writer fences, then one thread publishes with the atomics.
-  __threadfence();
   __syncthreads();
-  // Count this CTA done on every request its run touches; keep the ones it completes.
+  // Count this CTA done on every request its run touches; keep the ones it
+  // completes.  The acquire-release increments publish this CTA's block means
+  // and, for the CTA that completes a request, make every other CTA's visible.
   if (tid == 0) {
     const int r_first = owner_of(s.blk_off, s.R, b0), r_last = owner_of(s.blk_off, s.R, b1 - 1);
     int nsel = 0;
@@ -244,7 +254,7 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailArgs a) {
       const int f = s.blk_off[r], e = s.blk_off[r + 1];
       if (e == f) continue;   // empty request (no blocks)
       const int ctas = (e - 1) / a.bpc - f / a.bpc + 1;
-      if (atomicAdd(a.counters + r, 1) == ctas - 1) s_sel[nsel++] = r;
+      if (ctas == 1 || add_acq_rel(a.counters + r, 1) == ctas - 1) s_sel[nsel++] = r;
     }
     s_nsel = nsel;
   }
@@ -253,10 +263,9 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailArgs a) {
   if (nsel == 0) return;
   const SelectScratch sc = carve_select(s_dyn, a.nbp);
   for (int k = 0; k < nsel; ++k) select_and_emit(a, s_sel[k], sc);
-  __threadfence();
-  __syncthreads();
   if (tid == 0) {
-    if (atomicAdd(a.counters + s.R, nsel) + nsel == a.nonempty) s_last = 1;
+    // With one request (or this CTA completing all of them) nothing else is pending.
+    if (nsel == a.nonempty || add_acq_rel(a.counters + s.R, nsel) + nsel == a.nonempty) s_last = 1;
   }
   __syncthreads();
   if (s_last) finish_batch(a, false);
@@ -317,7 +326,7 @@ __global__ void __launch_bounds__(256) gather_list_kernel(const CompactArgs a, c
 }  // namespace
 
 int tail_blocks_per_cta(int G) {
-  int bpc = G > 0 ? 2048 / G : 1;
+  int bpc = G > 0 ? kTailThreads / G : 1;   // about one token per thread in the finalize phase
   return bpc < 1 ? 1 : (bpc > kTailMaxBpc ? kTailMaxBpc : bpc);
 }
 

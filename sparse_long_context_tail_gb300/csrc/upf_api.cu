@@ -283,7 +283,13 @@ upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p
     // Query rows per chunk: the whole group's tail rows when they fit the
     // tensor-core kernels' shared-memory budget (512 rows of d <= 128, 256 rows
     // of d = 256), rounded up to whole 128-row MMA tiles.
-    const int qc_max = pl->d <= 128 ? 512 : 256;
+    // At d = 256 a group of at most 256 rows is bound by the key reads (about
+    // QR flop per key byte, below the tensor/HBM ridge): chunks of 128 rows
+    // halve the resident queries, so the key ring holds two tiles instead of
+    // one and the next tile streams in while the current one is used (the
+    // second chunk's CTA finds the same keys in L2).
+    int qc_max = pl->d <= 128 ? 512 : 256;
+    if (pl->d == 256 && pl->QR <= 256) qc_max = 128;
     pl->QC = std::min(((pl->QR + 127) / 128) * 128, qc_max);
     pl->NQC = ceil_div(pl->QR, pl->QC);
     // Tensor-core kernels load tail rows in TMA boxes of 16..128 rows that
