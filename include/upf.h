@@ -167,12 +167,13 @@ upf_status upf_sync_status(upf_ctx* ctx, void* stream);
 size_t upf_workspace_bytes(const upf_batch* batch, const upf_params* params);
 
 /* Work split of the two scoring passes for this batch (inspection and tests;
- * no GPU needed): keys per split of pass 1 and pass 2 and the number of work
- * items (one CTA each) of each pass.  Any output may be NULL.  The tensor-core
- * passes run one CTA per SM, so the split is chosen by the estimated time of
- * the items over the device's 152 SMs.  Errors: as upf_workspace_bytes. */
+ * no GPU needed): keys per split of pass 1 and pass 2, the number of work
+ * items of each pass, and the CTAs that run one item (1, or 2 for a CTA pair
+ * sharing M = 256 MMAs).  Any output may be NULL.  The tensor-core passes run
+ * one CTA per SM, so the split is chosen by the estimated time of the items
+ * over the device's 152 SMs (76 pairs).  Errors: as upf_workspace_bytes. */
 upf_status upf_plan_info(const upf_batch* batch, const upf_params* params, int32_t* key_split1, int32_t* key_split2,
-                         int64_t* items1, int64_t* items2);
+                         int64_t* items1, int64_t* items2, int32_t* ctas_per_item);
 
 /* Tail-query importance of every token (section 二, first step; section 三,
  * scores + online normalisation):

@@ -19,8 +19,8 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libupf.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["upf_api.cu", "score_simt.cu", "score_tc.cu", "select.cu", "tail.cu", "compact.cu", "layers.cu",
-           "select_noalloc.cu"]
+SOURCES = ["upf_api.cu", "score_simt.cu", "score_tc.cu", "score_pair.cu", "select.cu", "tail.cu", "compact.cu",
+           "layers.cu", "select_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "-I" + INCLUDE, "-I" + CSRC,
               "--expt-relaxed-constexpr"]

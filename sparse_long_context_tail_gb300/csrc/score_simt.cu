@@ -252,7 +252,7 @@ cudaError_t launch_describe(const DescribeArgs& a, cudaStream_t s, bool pdl) {
 }
 
 cudaError_t launch_score_pass1(const ScoreArgs& a, cudaStream_t s, bool pdl) {
-  if (a.use_tc) return launch_score_pass1_tc(a, s, pdl);
+  if (a.use_tc) return a.use_pair ? launch_score_pass1_pair(a, s, pdl) : launch_score_pass1_tc(a, s, pdl);
   if (a.items1 == 0) return cudaSuccess;
   const size_t smem = pass1_smem(a.d);
   cudaError_t e = cudaFuncSetAttribute(score_pass1_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
@@ -261,7 +261,7 @@ cudaError_t launch_score_pass1(const ScoreArgs& a, cudaStream_t s, bool pdl) {
 }
 
 cudaError_t launch_score_pass2(const ScoreArgs& a, cudaStream_t s, bool pdl) {
-  if (a.use_tc) return launch_score_pass2_tc(a, s, pdl);
+  if (a.use_tc) return a.use_pair ? launch_score_pass2_pair(a, s, pdl) : launch_score_pass2_tc(a, s, pdl);
   if (a.items2 == 0) return cudaSuccess;
   const size_t smem = pass2_smem(a.d, a.QC);
   cudaError_t e = cudaFuncSetAttribute(score_pass2_simt, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));

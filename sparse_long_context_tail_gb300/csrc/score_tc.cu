@@ -40,6 +40,7 @@
 #include <climits>
 #include <cmath>
 
+#include "score_common.cuh"
 #include "sm100_ptx.cuh"
 #include "upf_internal.cuh"
 
@@ -65,10 +66,6 @@ constexpr int kSmemLimit = 232448;             // opt-in dynamic shared memory p
 // freed) always get the full limit; pipeline waits use ScoreArgs::wait_limit.
 constexpr long long kWaitLimit = kDefaultWaitCycles;
 constexpr uint32_t kIdleNs = 4000;              // longest suspension of a waiting role per poll
-
-__host__ __device__ constexpr int imin(int a, int b) { return a < b ? a : b; }
-__host__ __device__ constexpr int imax(int a, int b) { return a > b ? a : b; }
-__device__ __forceinline__ int ceil_div_dev(int a, int b) { return (a + b - 1) / b; }
 
 // Shape of one pass's pipeline for head dim d and QC query rows per chunk.
 struct Geo {
@@ -183,43 +180,6 @@ __device__ __forceinline__ void abort_with_timeout(const ScoreArgs& a, const Sme
   *reinterpret_cast<volatile int*>(sm.abort_flag) = 1;
 }
 
-__device__ __forceinline__ int find_owner(const int32_t* off, int R, int x) {
-  int lo = 0, hi = R - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (off[mid] <= x) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
-}
-
-// Work item: request r, kv head g, key split s, query chunk qc.  Items of one
-// request are numbered ((g * nsplit) + s) * NQC + qc, so the chunks that share
-// a key range are neighbours in the grid and read the range once from DRAM.
-struct ItemTC {
-  int r, g, qc, s, tok0, L;
-};
-
-__device__ __forceinline__ ItemTC locate_tc(const int32_t* item_off, const int32_t* cu, int R, int item, int KS,
-                                            int NQC) {
-  ItemTC it;
-  it.r = find_owner(item_off, R, item);
-  it.tok0 = cu[it.r];
-  it.L = cu[it.r + 1] - it.tok0;
-  const int nsplit = ceil_div_dev(it.L, KS);
-  int local = item - item_off[it.r];
-  it.qc = local % NQC;
-  local /= NQC;
-  it.s = local % nsplit;
-  it.g = local / nsplit;
-  return it;
-}
-
-__device__ __forceinline__ int64_t item_index(const int32_t* item_off, int r, int g, int s, int qc, int nsplit,
-                                              int NQC) {
-  return item_off[r] + ((int64_t)g * nsplit + s) * NQC + qc;
-}
-
 // Rows of the query chunk present in this item: [0, rows_c).
 __device__ __forceinline__ int chunk_rows(const ScoreArgs& a, int qc) { return min(a.QC, a.QR - qc * a.QC); }
 
@@ -231,88 +191,6 @@ __device__ __forceinline__ void zero_padding(const ScoreArgs& a, const Smem& sm,
     uint4* base = reinterpret_cast<uint4*>(sm.q + size_t(s) * a.QC * 128 + size_t(rows_c) * 128);
     for (int i = threadIdx.x; i < n16; i += blockDim.x) base[i] = make_uint4(0, 0, 0, 0);
   }
-}
-
-// ------------------------------------------------------- epilogue math -----
-
-// sum_j 2^(v[j] * sl - ref) over 32 values, with the affine step and the
-// accumulation in packed fp32 pairs.
-__device__ __forceinline__ float exp_sum32(const float (&v)[32], float sl, float ref) {
-  const uint64_t sl2 = pack2(sl, sl), nm2 = pack2(-ref, -ref);
-  uint64_t acc0 = pack2(0.f, 0.f), acc1 = pack2(0.f, 0.f);
-#pragma unroll
-  for (int j = 0; j < 32; j += 4) {
-    float a, b, c, d;
-    unpack2(fma2(pack2(v[j], v[j + 1]), sl2, nm2), a, b);
-    unpack2(fma2(pack2(v[j + 2], v[j + 3]), sl2, nm2), c, d);
-    acc0 = add2(acc0, pack2(ex2_approx(a), ex2_approx(b)));
-    acc1 = add2(acc1, pack2(ex2_approx(c), ex2_approx(d)));
-  }
-  float lo, hi;
-  unpack2(add2(acc0, acc1), lo, hi);
-  return lo + hi;
-}
-
-__device__ __forceinline__ float max32(const float (&v)[32]) {
-  float t[11];
-#pragma unroll
-  for (int j = 0; j < 10; ++j) t[j] = max3(v[3 * j], v[3 * j + 1], v[3 * j + 2]);
-  t[10] = fmaxf(v[30], v[31]);
-  return fmaxf(max3(max3(t[0], t[1], t[2]), max3(t[3], t[4], t[5]), max3(t[6], t[7], t[8])), fmaxf(t[9], t[10]));
-}
-
-__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
-  float4 r;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "r"(addr));
-  return r;
-}
-
-// Pass 1 folds the logits of one query row (raw dot products; invisible
-// entries -inf) into its running (m, Z), m and the exponents in log2 units
-// scaled by sl = scale * log2(e), Z = sum 2^(x*sl - m).  m is a reference
-// point, not the running maximum: the exponentials are taken against the
-// current m, and only a unit whose chunk sums leave [0, 2^20] (a term above
-// about 2^15, an overflow, or the first visible chunk, where m is -inf and a
-// sum is inf or NaN) takes this slow step, which moves m to the maximum of the
-// unit's CPW chunks (if above m) and rescales Z.  m + log2 Z is the same
-// either way.
-template <int CPW>
-__device__ __forceinline__ void online_rescale(const float (&va)[32], const float (&vb)[32], float sl, float& m,
-                                               float& z) {
-  const float mx = (CPW == 2 ? fmaxf(max32(va), max32(vb)) : max32(va)) * sl;
-  if (mx == -INFINITY) return;        // nothing visible
-  const float mn = fmaxf(m, mx);
-  float sum = exp_sum32(va, sl, mn);
-  if (CPW == 2) sum += exp_sum32(vb, sl, mn);
-  z = z * ex2_approx(m - mn) + sum;
-  m = mn;
-}
-
-// Pass-2 step, unmasked: acc += 2^(v * sl - lse2) over 32 query columns of one
-// key; nlse is the shared-memory address of -lse2 of those columns (16-byte
-// aligned).
-__device__ __forceinline__ void normalised_sum32(const float (&v)[32], uint32_t nlse, float sl, uint64_t& acc0,
-                                                 uint64_t& acc1) {
-  const uint64_t sl2 = pack2(sl, sl);
-#pragma unroll
-  for (int j = 0; j < 32; j += 4) {
-    const float4 l = lds_f4(nlse + 4 * j);
-    float a, b, c, d;
-    unpack2(fma2(pack2(v[j], v[j + 1]), sl2, pack2(l.x, l.y)), a, b);
-    unpack2(fma2(pack2(v[j + 2], v[j + 3]), sl2, pack2(l.z, l.w)), c, d);
-    acc0 = add2(acc0, pack2(ex2_approx(a), ex2_approx(b)));
-    acc1 = add2(acc1, pack2(ex2_approx(c), ex2_approx(d)));
-  }
-}
-
-// The same near the causal edge: only the columns whose query sees the key.
-__device__ __forceinline__ float normalised_sum32_masked(const float (&v)[32], const float* nlse, const int* tq,
-                                                         int key, float sl) {
-  float acc = 0.f;
-#pragma unroll
-  for (int j = 0; j < 32; ++j)
-    if (key <= tq[j]) acc += ex2_approx(fmaf(v[j], sl, nlse[j]));
-  return acc;
 }
 
 // An epilogue warp is done reading a TMEM slot: order its loads before the
@@ -856,38 +734,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 }
 
 // ------------------------------------------------------------- host -------
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-// 3-D bf16 map over [T, H, d] rows (row stride `stride` elements): box of 64
-// dims x 1 head x `rows` tokens, 128-byte swizzle.
-cudaError_t make_map(CUtensorMap* m, const void* base, int d, int H, int T, int64_t stride, int rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return cudaErrorNotSupported;
-  cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(H), cuuint64_t(T > 0 ? T : 1)};
-  cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(stride) * 2};
-  cuuint32_t box[3] = {64, 1, cuuint32_t(rows)};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
 
 template <class K>
 cudaError_t launch_pass(K kernel, int pass, int items, const ScoreArgs& a, cudaStream_t s, bool pdl) {

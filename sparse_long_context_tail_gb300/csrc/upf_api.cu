@@ -85,6 +85,7 @@ struct Plan {
   int pw = 1;   // partial rows per pass-1 item row and per (kv head, query chunk)
   int q_box_rows = 0;
   bool use_tc = false;
+  bool use_pair = false;
   long long items1 = 0, items2 = 0;
   long long NB = 0;
   int max_nb = 0;
@@ -236,6 +237,19 @@ int choose_split_tc(const upf_batch* b, int hkv, int nqc, int tile, int sms) {
     if (e.ks && e.key == key) return e.ks;
   const long long ovh = 2LL * tile;
   long long best_t = split_makespan(b, hkv, nqc, best, ovh, sms);
+  // a geometric sweep around the ideal split (uneven request lengths make
+  // the best split hard to predict) ...
+  const long long ideal = (keys * units + sms - 1) / sms;
+  for (int i = 0; i < 25; ++i) {
+    // 1/8 x .. 2 x in steps of 2^(1/6)
+    const long long ks = std::min(hi_ks, round_tile((long long)(double(ideal) * std::exp2(i / 6.0 - 3.0))));
+    const long long t = split_makespan(b, hkv, nqc, ks, ovh, sms);
+    if (t < best_t || (t == best_t && ks > best)) {
+      best_t = t;
+      best = ks;
+    }
+  }
+  // ... and the smallest splits that fit the items into 1..4 waves
   for (int w = 1; w <= 4; ++w) {
     // smallest whole-tile split with at most w * sms items (items fall as the split grows)
     long long lo = round_tile((keys * units + (long long)w * sms - 1) / ((long long)w * sms)), hi = hi_ks;
@@ -308,7 +322,15 @@ upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p
     // depends only on the batch and parameters (never on the device), so
     // upf_workspace_bytes() without a context sizes exactly what a call uses.
     (void)ctx;
-    if (pl->use_tc) {
+    // Chunks of whole 256-row units run on CTA pairs (one M = 256 MMA over two
+    // SMs); UPF_SCORE_PAIRS=0 keeps them on single CTAs (used by tests to
+    // cross-check the two).
+    const char* pairs = std::getenv("UPF_SCORE_PAIRS");
+    pl->use_pair = pl->use_tc && pl->QC % 256 == 0 && !(pairs && std::strcmp(pairs, "0") == 0);
+    if (pl->use_pair) {
+      pl->KS1 = choose_split_tc(b, pl->Hkv, pl->NQC, upf::kPairTileKeys, upf::kPlanSMs / 2);
+      pl->KS2 = choose_split_tc(b, pl->Hkv, pl->NQC, upf::kPairTileKeys, upf::kPlanSMs / 2);
+    } else if (pl->use_tc) {
       pl->KS1 = choose_split_tc(b, pl->Hkv, pl->NQC, upf::score_tc_key_tile(1, pl->d), upf::kPlanSMs);
       pl->KS2 = choose_split_tc(b, pl->Hkv, pl->NQC, upf::score_tc_key_tile(2, pl->d), upf::kPlanSMs);
     } else {
@@ -461,6 +483,7 @@ upf::ScoreArgs score_args(const upf_ctx* ctx, const upf_batch* b, const Plan& pl
   a.scale_log2 = pl.scale * 1.4426950408889634f;
   a.q_box_rows = pl.q_box_rows;
   a.use_tc = pl.use_tc ? 1 : 0;
+  a.use_pair = pl.use_pair ? 1 : 0;
   a.item_off1 = at<int32_t>(ws, pl.off_desc);
   a.item_off2 = at<int32_t>(ws, pl.off_desc) + (pl.R + 1);
   a.pw = pl.pw;
@@ -773,7 +796,7 @@ static upf_status score_impl(upf_ctx* ctx, const upf_batch* batch, const upf_par
 }
 
 upf_status upf_plan_info(const upf_batch* batch, const upf_params* params, int32_t* key_split1, int32_t* key_split2,
-                         int64_t* items1, int64_t* items2) {
+                         int64_t* items1, int64_t* items2, int32_t* ctas_per_item) {
   Plan pl;
   upf_status st = make_plan(nullptr, batch, params, true, &pl);
   if (st != UPF_OK) return st;
@@ -781,6 +804,7 @@ upf_status upf_plan_info(const upf_batch* batch, const upf_params* params, int32
   if (key_split2) *key_split2 = pl.KS2;
   if (items1) *items1 = pl.items1;
   if (items2) *items2 = pl.items2;
+  if (ctas_per_item) *ctas_per_item = pl.use_pair ? 2 : 1;
   return UPF_OK;
 }
 

@@ -48,6 +48,7 @@ struct ScoreArgs {
   float scale_log2;
   int32_t q_box_rows;        // tail rows per TMA box of q (divides n)
   int32_t use_tc;            // 1: tcgen05 kernels, 0: CUDA-core kernels
+  int32_t use_pair;          // 1: the tcgen05 kernels on CTA pairs (cta_group::2)
   const int32_t* item_off1;  // [R+1]
   const int32_t* item_off2;  // [R+1]
   float2* p1part;            // [items1][pw][QC]
@@ -181,6 +182,10 @@ cudaError_t launch_score_pass1(const ScoreArgs& a, cudaStream_t s, bool pdl = fa
 cudaError_t launch_score_pass2(const ScoreArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_score_pass1_tc(const ScoreArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_score_pass2_tc(const ScoreArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_score_pass1_pair(const ScoreArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_score_pass2_pair(const ScoreArgs& a, cudaStream_t s, bool pdl = false);
+size_t score_pair_smem_bytes(int pass, int d, int QC);
+constexpr int kPairTileKeys = 256;   // keys per tile of a CTA pair (key splits are multiples)
 // Dynamic shared memory of a tensor-core pass (1 or 2) for head dim d and QC
 // rows per query chunk, and its keys per tile (key splits are multiples of it).
 size_t score_tc_smem_bytes(int pass, int d, int QC);

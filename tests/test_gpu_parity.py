@@ -150,6 +150,27 @@ def test_cuda_core_fallback_parity(sel, name, c, monkeypatch):
     check(w, p, out, status, inputs)
 
 
+@pytest.mark.parametrize("name,c", [SMALL[1], SMALL[2]], ids=["llama-2req", "qwen-n512-G32"])
+def test_single_cta_scoring_parity(sel, name, c, monkeypatch):
+    """Chunks of whole 256-row units run on CTA pairs by default; the one-CTA
+    tensor-core kernels (UPF_SCORE_PAIRS=0) must match the oracle as well."""
+    monkeypatch.setenv("UPF_SCORE_PAIRS", "0")
+    spec = small_spec(name, c)
+    w = wl.generate(spec)
+    p = params_of(spec)
+    out, status, inputs = run_gpu(sel, w, p)
+    check(w, p, out, status, inputs)
+
+
+def test_single_cta_scoring_full_size(sel, monkeypatch):
+    monkeypatch.setenv("UPF_SCORE_PAIRS", "0")
+    spec = wl.named_spec("llama8b-L131072")
+    w = wl.generate(spec)
+    p = params_of(spec)
+    out, status, inputs = run_gpu(sel, w, p)
+    check(w, p, out, status, inputs)
+
+
 def test_odd_tail_count_uses_fallback(sel):
     """n = 100 (not a multiple of 16) runs on the CUDA-core kernels."""
     spec = wl.WorkloadSpec("n100", [900, 2048], 8, 2, 128, 256, n_tail=100, block=64, planted=[1, 2], seed=9)
