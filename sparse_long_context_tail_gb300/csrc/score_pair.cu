@@ -56,6 +56,7 @@ constexpr int kNumBars = 3 * kMaxStages + 2 * kSlots + 3;
 constexpr int kSmemLimit = 232448;
 constexpr long long kWaitLimit = kDefaultWaitCycles;
 constexpr uint32_t kIdleNs = 4000;
+constexpr uint32_t kRemoteNs = 64;   // polls of phases that the peer CTA completes
 
 struct PGeo {
   int S;            // 64-wide slices of the head dim
@@ -265,7 +266,7 @@ __device__ void pair_mma(const ScoreArgs& a, const PSmem& sm, const PGeo& geo, i
   const uint32_t q_slice = uint32_t(geo.U * kHalf) * 128u;
   const uint32_t q_unit = uint32_t(kHalf) * 128u;
   bool ok = mbar_wait_idle(b_qfull(sm), 0, a.wait_limit, kIdleNs) &&
-            mbar_wait_cluster(b_pqfull(sm), 0, a.wait_limit, kIdleNs);
+            mbar_wait_cluster(b_pqfull(sm), 0, a.wait_limit, kRemoteNs);
   int st = 0, slot = 0;
   uint32_t ph = 0, sph = 0;
   for (int i = 0; ok && i < ntiles; ++i) {
@@ -276,17 +277,17 @@ __device__ void pair_mma(const ScoreArgs& a, const PSmem& sm, const PGeo& geo, i
     const int st0 = st, st1 = st + 1 == geo.NS ? 0 : st + 1;
     const uint32_t ph1 = st1 == 0 ? ph ^ 1u : ph;
     ok = mbar_wait_idle(b_full(sm, st0), ph, a.wait_limit, kIdleNs) &&
-         mbar_wait_cluster(b_pfull(sm, st0), ph, a.wait_limit, kIdleNs);
+         mbar_wait_cluster(b_pfull(sm, st0), ph, a.wait_limit, kRemoteNs);
     if (ok && geo.spt == 2)
       ok = mbar_wait_idle(b_full(sm, st1), ph1, a.wait_limit, kIdleNs) &&
-           mbar_wait_cluster(b_pfull(sm, st1), ph1, a.wait_limit, kIdleNs);
+           mbar_wait_cluster(b_pfull(sm, st1), ph1, a.wait_limit, kRemoteNs);
     if (geo.spt == 2) { st = st1 + 1 == geo.NS ? 0 : st1 + 1; ph = (st1 == 0 || st == 0) ? ph ^ 1u : ph; }
     else { st = st1; ph = st1 == 0 ? ph ^ 1u : ph; }
     if (!ok) break;
     tc_fence_after();
     const uint32_t k0a = ring0 + uint32_t(st0 * geo.stage_bytes), k1a = ring0 + uint32_t(st1 * geo.stage_bytes);
     for (int u = 0; u < U; ++u) {
-      ok = mbar_wait_cluster(b_tempty(sm, slot), sph ^ 1u, a.wait_limit, kIdleNs);
+      ok = mbar_wait_cluster(b_tempty(sm, slot), sph ^ 1u, a.wait_limit, kRemoteNs);
       if (!ok) break;
       tc_fence_after();
       const uint32_t dt = tmem + uint32_t(slot * 256);
@@ -332,7 +333,8 @@ __device__ __forceinline__ bool pair_wait_slot(const ScoreArgs& a, const PSmem& 
     return true;
   }
   if (paborted(sm)) return false;
-  if (!mbar_wait_idle(b_tfull(sm, slot), parity, a.wait_limit, kIdleNs)) {
+  // CTA 1's slots are filled by CTA 0's multicast commit: short polls there.
+  if (!mbar_wait_idle(b_tfull(sm, slot), parity, a.wait_limit, rank ? kRemoteNs : kIdleNs)) {
     pabort(a, sm, rank);
     return false;
   }

@@ -283,6 +283,9 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
   return ok != 0;
 }
 
+// Phases completed by another CTA's remote arrive are waited for with a short
+// suspension per poll (`ns`, e.g. 64): a remote arrive is not relied on to
+// wake a suspended thread early.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, long long limit, uint32_t ns) {
   if (mbar_test_cluster(bar, parity)) return true;
   const long long t0 = clock64();
