@@ -322,11 +322,18 @@ upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p
     // depends only on the batch and parameters (never on the device), so
     // upf_workspace_bytes() without a context sizes exactly what a call uses.
     (void)ctx;
-    // Chunks of whole 256-row units run on CTA pairs (one M = 256 MMA over two
-    // SMs); UPF_SCORE_PAIRS=0 keeps them on single CTAs (used by tests to
-    // cross-check the two).
+    // At d = 256, chunks of whole 256-row units run on CTA pairs (one M = 256
+    // MMA over two SMs): each SM holds half of the 128 KB query chunk and
+    // reads 8 instead of 12 KB of operands per 128 MMA clocks, which the
+    // d = 256 passes (MMA-bound, two 64 KB key tiles) need; measured 21-26 %
+    // faster there.  At d <= 128 the exponentials match the MMA rate and the
+    // pair, whose MMA waits for both CTAs' epilogues, was measured 45 %
+    // slower, so those stay on single CTAs.  UPF_SCORE_PAIRS=0 keeps every
+    // chunk on single CTAs, =1 allows pairs at any d (tests cross-check both).
     const char* pairs = std::getenv("UPF_SCORE_PAIRS");
-    pl->use_pair = pl->use_tc && pl->QC % 256 == 0 && !(pairs && std::strcmp(pairs, "0") == 0);
+    const bool pairs_off = pairs && std::strcmp(pairs, "0") == 0;
+    const bool pairs_any_d = pairs && std::strcmp(pairs, "1") == 0;
+    pl->use_pair = pl->use_tc && pl->QC % 256 == 0 && !pairs_off && (pl->d == 256 || pairs_any_d);
     if (pl->use_pair) {
       pl->KS1 = choose_split_tc(b, pl->Hkv, pl->NQC, upf::kPairTileKeys, upf::kPlanSMs / 2);
       pl->KS2 = choose_split_tc(b, pl->Hkv, pl->NQC, upf::kPairTileKeys, upf::kPlanSMs / 2);

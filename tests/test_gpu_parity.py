@@ -150,11 +150,14 @@ def test_cuda_core_fallback_parity(sel, name, c, monkeypatch):
     check(w, p, out, status, inputs)
 
 
-@pytest.mark.parametrize("name,c", [SMALL[1], SMALL[2]], ids=["llama-2req", "qwen-n512-G32"])
-def test_single_cta_scoring_parity(sel, name, c, monkeypatch):
-    """Chunks of whole 256-row units run on CTA pairs by default; the one-CTA
-    tensor-core kernels (UPF_SCORE_PAIRS=0) must match the oracle as well."""
-    monkeypatch.setenv("UPF_SCORE_PAIRS", "0")
+@pytest.mark.parametrize("pairs", ["0", "1"])
+@pytest.mark.parametrize("name,c", [SMALL[1], SMALL[2], SMALL[0]], ids=["llama-2req", "qwen-n512-G32", "ragged-d64"])
+def test_scoring_on_single_ctas_and_on_pairs(sel, name, c, pairs, monkeypatch):
+    """d = 256 chunks of whole 256-row units run on CTA pairs by default, the
+    rest on single CTAs; both kernel families must match the oracle at every
+    head dim (UPF_SCORE_PAIRS=0: single CTAs only, =1: pairs wherever the
+    chunk allows)."""
+    monkeypatch.setenv("UPF_SCORE_PAIRS", pairs)
     spec = small_spec(name, c)
     w = wl.generate(spec)
     p = params_of(spec)
@@ -162,8 +165,8 @@ def test_single_cta_scoring_parity(sel, name, c, monkeypatch):
     check(w, p, out, status, inputs)
 
 
-def test_single_cta_scoring_full_size(sel, monkeypatch):
-    monkeypatch.setenv("UPF_SCORE_PAIRS", "0")
+def test_pair_scoring_full_size_at_d128(sel, monkeypatch):
+    monkeypatch.setenv("UPF_SCORE_PAIRS", "1")
     spec = wl.named_spec("llama8b-L131072")
     w = wl.generate(spec)
     p = params_of(spec)
