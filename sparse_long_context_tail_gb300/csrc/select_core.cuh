@@ -76,15 +76,26 @@ __device__ __forceinline__ T sel_block_sum(T v, T* s_tmp) {
   return t;
 }
 
-// Adds `mass` to hist[digit] for every lane with digit < 256.  Every lane of
-// the warp calls it (lanes with nothing to add pass digit >= 256).  Up to four
-// times, the lanes sharing the digit of the lowest lane still pending add
-// their masses with two full-warp reductions of 24-bit halves (no sum
-// overflows 32 bits) and one lane does a single shared atomic; lanes left
-// after that (digits already spread out) add their own.
-__device__ __forceinline__ void hist_add_aggregated(unsigned long long* hist, uint32_t digit,
-                                                    unsigned long long mass) {
+// Mass histograms are kept as three 32-bit histograms of the masses' 16-bit
+// parts (native 32-bit shared atomics; a bucket's part sum stays below
+// 16384 * 2^16 = 2^30), combined when the buckets are scanned.
+struct MassHist {
+  uint32_t p[3][256];
+};
+
+__device__ __forceinline__ unsigned long long hist_mass(const MassHist& h, int d) {
+  return (unsigned long long)h.p[0][d] + ((unsigned long long)h.p[1][d] << 16) + ((unsigned long long)h.p[2][d] << 32);
+}
+
+// Adds `mass` to bucket `digit` for every lane with digit < 256.  Every lane
+// of the warp calls it (lanes with nothing to add pass digit >= 256).  Up to
+// four times, the lanes sharing the digit of the lowest lane still pending add
+// their masses with full-warp reductions of the 16-bit parts (no sum overflows
+// 32 bits) and one lane does the shared atomics; lanes left after that (digits
+// already spread out) add their own.
+__device__ __forceinline__ void hist_add_aggregated(MassHist& h, uint32_t digit, unsigned long long mass) {
   const int lane = threadIdx.x & 31;
+  const uint32_t m0 = uint32_t(mass & 0xFFFFull), m1 = uint32_t((mass >> 16) & 0xFFFFull), m2 = uint32_t(mass >> 32);
   unsigned pending = __ballot_sync(0xffffffffu, digit < 256u);
 #pragma unroll 1
   for (int it = 0; it < 4 && pending; ++it) {
@@ -92,12 +103,21 @@ __device__ __forceinline__ void hist_add_aggregated(unsigned long long* hist, ui
     const uint32_t d = __shfl_sync(0xffffffffu, digit, leader);
     const bool mine = ((pending >> lane) & 1u) && digit == d;
     const unsigned group = __ballot_sync(0xffffffffu, mine);
-    const uint32_t lo = __reduce_add_sync(0xffffffffu, mine ? uint32_t(mass & 0xFFFFFFull) : 0u);
-    const uint32_t hi = __reduce_add_sync(0xffffffffu, mine ? uint32_t(mass >> 24) : 0u);
-    if (lane == leader) atomicAdd(&hist[d], (unsigned long long)lo + ((unsigned long long)hi << 24));
+    const uint32_t s0 = __reduce_add_sync(0xffffffffu, mine ? m0 : 0u);
+    const uint32_t s1 = __reduce_add_sync(0xffffffffu, mine ? m1 : 0u);
+    const uint32_t s2 = __reduce_add_sync(0xffffffffu, mine ? m2 : 0u);
+    if (lane == leader) {
+      atomicAdd(&h.p[0][d], s0);
+      atomicAdd(&h.p[1][d], s1);
+      atomicAdd(&h.p[2][d], s2);
+    }
     pending &= ~group;
   }
-  if ((pending >> lane) & 1u) atomicAdd(&hist[digit], mass);
+  if ((pending >> lane) & 1u) {
+    atomicAdd(&h.p[0][digit], m0);
+    atomicAdd(&h.p[1][digit], m1);
+    atomicAdd(&h.p[2][digit], m2);
+  }
 }
 
 // Selects the blocks of one request: block scores bs[0..nb) (global, any
@@ -107,7 +127,7 @@ __device__ __forceinline__ void hist_add_aggregated(unsigned long long* hist, ui
 // score keeps the whole request and records UPF_ERR_NONFINITE.
 static __device__ int select_request(const float* bs, int nb, int L, int G, float top_p, int sink_keep, int tail_keep,
                               const SelectScratch& sc, int32_t* status) {
-  __shared__ unsigned long long h_mass[2][256];   // this round's histogram and the next one's, cleared meanwhile
+  __shared__ MassHist h_mass[2];   // this round's histogram and the next one's, cleared meanwhile
   __shared__ unsigned long long s_u64[kSelWarps];
   __shared__ float s_f[kSelWarps];
   __shared__ int s_i[kSelWarps];
@@ -152,7 +172,7 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
       sc.m[i] = m;
       part += m;
     }
-    for (int d = tid; d < 256; d += blockDim.x) h_mass[0][d] = 0;   // ordered by the barriers in the sum
+    for (int d = tid; d < 3 * 256; d += blockDim.x) (&h_mass[0].p[0][0])[d] = 0;   // ordered by the barriers in the sum
     const unsigned long long total = sel_block_sum(part, s_u64);
     // Mass the selected prefix must reach: the smallest integer >= top_p * total.
     const unsigned long long target = (unsigned long long)ceil((double)top_p * (double)total);
@@ -162,7 +182,7 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
       const int nb_pad = (nb + 31) & ~31;   // whole warps take part in the aggregation
       int cur = 0;
       for (int shift = 24; shift >= 0; shift -= 8, cur ^= 1) {
-        unsigned long long* hist = h_mass[cur];
+        MassHist& hist = h_mass[cur];
         for (int i = tid; i < nb_pad; i += blockDim.x) {
           uint32_t digit = 256u + lane;        // nothing to add
           unsigned long long m = 0;
@@ -181,7 +201,7 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
           unsigned long long loc[8], lsum = 0;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            loc[j] = hist[255 - 8 * lane - j];
+            loc[j] = hist_mass(hist, 255 - 8 * lane - j);
             lsum += loc[j];
           }
           unsigned long long incl = lsum;
@@ -207,8 +227,8 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
             s_digit = dsel;
             s_above = run;
           }
-        } else if (tid < 32 + 256) {
-          h_mass[cur ^ 1][tid - 32] = 0;   // the next round's histogram
+        } else if (tid < 32 + 3 * 256) {
+          (&h_mass[cur ^ 1].p[0][0])[tid - 32] = 0;   // the next round's histogram
         }
         __syncthreads();
         prefix |= uint32_t(s_digit) << shift;

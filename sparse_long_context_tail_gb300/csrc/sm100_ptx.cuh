@@ -99,6 +99,19 @@ __device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity, lo
   return true;
 }
 
+// mbar_wait_idle that also gives up (false) once *abort becomes non-zero; the
+// flag is read only while the phase is pending, so an uncontended wait costs
+// nothing extra.
+__device__ __forceinline__ bool mbar_wait_idle_abortable(uint32_t bar, uint32_t parity, long long limit, uint32_t ns,
+                                                         const int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_hint(bar, parity, ns)) {
+    if (*reinterpret_cast<const volatile int*>(abort) != 0 || clock64() - t0 > limit) return false;
+  }
+  return true;
+}
+
 // ----------------------------------------------------------------- TMA ----
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int c0, int c1, uint32_t bar) {

@@ -15,9 +15,8 @@
 // the given score) and each block's mean.  Then each CTA counts itself done on
 // every request its run touches (one atomic per request); the CTA that
 // completes a request runs that request's selection (select_core.cuh) with all
-// its threads, writes the request's keep bits, its kept count and the packed
-// indices of its kept tokens (at the request's own offset in a list), and
-// counts the request done.  The CTA that completes the last request writes
+// its threads, writes the request's keep bits, its kept count and the list of
+// its kept blocks with their output offsets, and counts the request done.  The CTA that completes the last request writes
 // the compacted batch offsets, the total, the keep-bit words shared by
 // neighbouring requests, and zero counts for empty requests.  Nothing waits:
 // completion is detected with fenced atomics, so there is no spin anywhere.
@@ -122,7 +121,7 @@ __device__ void finish_batch(const TailArgs& a, bool no_blocks) {
 // inside the request by plain stores, the first and last word's bits to the
 // edge scratch), its count and its kept-token list.
 __device__ void select_and_emit(const TailArgs& a, int r, const SelectScratch& sc) {
-  __shared__ int s_warp[kTailWarps];
+  __shared__ int s_warp[kTailWarps], s_warpb[kTailWarps];
   const SelectArgs& s = a.s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b0 = s.blk_off[r], nb = s.blk_off[r + 1] - b0;
@@ -138,37 +137,46 @@ __device__ void select_and_emit(const TailArgs& a, int r, const SelectScratch& s
       a.edge_bits[2 * r + (w == w0 ? 0 : 1)] = bits;
     }
   }
-  if (a.kept_list) {
-    // Output offset of every block (exclusive prefix of kept block sizes in
-    // block order), into sc.bits (free after the selection); thread t owns the
-    // contiguous blocks [t*per, (t+1)*per).
-    uint32_t* off = sc.bits;
+  if (a.kept_blk) {
+    // The kept blocks in order with their output offsets inside the request
+    // (exclusive prefix of kept block sizes); thread t owns the contiguous
+    // blocks [t*per, (t+1)*per).  The gather expands them to token rows.
     const int per = (nb + blockDim.x - 1) / blockDim.x;
     const int i0 = min(nb, tid * per), i1 = min(nb, i0 + per);
-    int mine = 0;
-    for (int i = i0; i < i1; ++i) mine += sc.keep[i] ? min(L, (i + 1) * s.G) - i * s.G : 0;
-    int incl = mine;
+    int mine = 0, mineb = 0;
+    for (int i = i0; i < i1; ++i)
+      if (sc.keep[i]) {
+        mine += min(L, (i + 1) * s.G) - i * s.G;
+        ++mineb;
+      }
+    int incl = mine, inclb = mineb;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
+      const int tb = __shfl_up_sync(0xffffffffu, inclb, o);
+      if (lane >= o) {
+        incl += t;
+        inclb += tb;
+      }
     }
-    if (lane == 31) s_warp[warp] = incl;
+    if (lane == 31) {
+      s_warp[warp] = incl;
+      s_warpb[warp] = inclb;
+    }
     __syncthreads();
-    int run = incl - mine;
-    for (int w = 0; w < warp; ++w) run += s_warp[w];
-    for (int i = i0; i < i1; ++i) {
-      off[i] = uint32_t(run);
-      run += sc.keep[i] ? min(L, (i + 1) * s.G) - i * s.G : 0;
+    int run = incl - mine, runb = inclb - mineb;
+    for (int w = 0; w < warp; ++w) {
+      run += s_warp[w];
+      runb += s_warpb[w];
     }
-    __syncthreads();
-    // one warp per kept block: its tokens' packed indices, coalesced
-    for (int i = warp; i < nb; i += kTailWarps) {
-      if (!sc.keep[i]) continue;
-      const int lo = i * s.G, n = min(L, lo + s.G) - lo;
-      int32_t* dst = a.kept_list + tok0 + off[i];
-      for (int j = lane; j < n; j += 32) dst[j] = tok0 + lo + j;
-    }
+    for (int i = i0; i < i1; ++i)
+      if (sc.keep[i]) {
+        a.kept_blk[b0 + runb] = i;
+        a.kept_off[b0 + runb] = run;
+        run += min(L, (i + 1) * s.G) - i * s.G;
+        ++runb;
+      }
+    if (tid == blockDim.x - 1) a.kept_nblk[r] = runb;
   }
   if (tid == 0) s.kept_count[r] = kept;   // read by the CTA that finishes the batch
   __syncthreads();
@@ -272,12 +280,15 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailArgs a) {
 }
 
 // The gather of the fused path: output row o belongs to the request r with
-// cu_out[r] <= o < cu_out[r+1]; its input row is entry o - cu_out[r] of r's
-// kept-token list.  One warp per output row, 16-byte vectors, eight in
-// flight per lane; block 0 appends the drop-history record.
-__global__ void __launch_bounds__(256) gather_list_kernel(const CompactArgs a, const int32_t* kept_list) {
+// cu_out[r] <= o < cu_out[r+1]; its kept block is the last one of r's list
+// whose output offset is <= o - cu_out[r] (binary search; every lane does the
+// same loads), and its input row follows from the block's first token.  One
+// warp per output row, 16-byte vectors, eight in flight per lane; block 0
+// appends the drop-history record.
+__global__ void __launch_bounds__(256) gather_list_kernel(const GatherListArgs g) {
   pdl_trigger();
   pdl_wait();
+  const CompactArgs& a = g.c;
   const int total = min(*a.total_kept, a.T);
   if (blockIdx.x == 0 && threadIdx.x == 0 && a.history) {
     bool full = false;
@@ -300,10 +311,17 @@ __global__ void __launch_bounds__(256) gather_list_kernel(const CompactArgs a, c
   const int64_t nvec = a.row_bytes / 16;
   for (int o = warp; o < total; o += nwarps) {
     const int r = owner_of(a.cu_out, a.R, o);
-    const int at = a.cu[r] + (o - a.cu_out[r]);
-    if (at < 0 || at >= a.T) continue;   // never for a consistent batch; no access outside the buffers
-    const int t = kept_list[at];
-    if (t < 0 || t >= a.T) continue;
+    const int j = o - a.cu_out[r];
+    const int base = g.blk_off[r];
+    int lo = 0, hi = g.kept_nblk[r] - 1;
+    if (hi < 0) continue;   // never for a consistent batch
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (g.kept_off[base + mid] <= j) lo = mid;
+      else hi = mid - 1;
+    }
+    const int t = a.cu[r] + g.kept_blk[base + lo] * g.G + (j - g.kept_off[base + lo]);
+    if (t < a.cu[r] || t >= a.cu[r + 1] || t >= a.T) continue;   // never for a consistent batch
     if (lane == 0 && a.kept_index) a.kept_index[o] = t;
     if (a.hidden_in) {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(a.hidden_in) + (int64_t)t * a.row_bytes);
@@ -345,10 +363,10 @@ cudaError_t launch_tail(const TailArgs& a, cudaStream_t s, bool pdl) {
   return launch_kernel(tail_kernel, grid, kTailThreads, smem, s, pdl, a);
 }
 
-cudaError_t launch_gather_list(const CompactArgs& a, const int32_t* kept_list, cudaStream_t s, bool pdl) {
-  int blocks = (a.T + 7) / 8;
+cudaError_t launch_gather_list(const GatherListArgs& a, cudaStream_t s, bool pdl) {
+  int blocks = (a.c.T + 7) / 8;
   blocks = blocks < 1 ? 1 : (blocks > 8 * kPlanSMs ? 8 * kPlanSMs : blocks);
-  return launch_kernel(gather_list_kernel, blocks, 256, 0, s, pdl, a, kept_list);
+  return launch_kernel(gather_list_kernel, blocks, 256, 0, s, pdl, a);
 }
 
 }  // namespace upf

@@ -92,7 +92,8 @@ struct Plan {
   int nwords = 0, nchunks = 0;
   std::vector<int32_t> qhead;
   // workspace offsets
-  size_t off_desc = 0, off_p1 = 0, off_part = 0, off_bs = 0, off_chunk = 0, off_kidx = 0, off_ctr = 0, total = 0;
+  size_t off_desc = 0, off_p1 = 0, off_part = 0, off_bs = 0, off_chunk = 0, off_kidx = 0, off_ctr = 0, off_kbl = 0,
+         total = 0;
   int nonempty = 0;
 };
 
@@ -384,6 +385,8 @@ upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p
   off = align256(off + sizeof(int32_t) * size_t(pl->T));
   pl->off_ctr = off;   // tail counters [R+1], then edge words [2R]
   off = align256(off + sizeof(int32_t) * size_t(pl->R + 1) + sizeof(uint32_t) * 2 * size_t(pl->R));
+  pl->off_kbl = off;   // kept blocks [NB], their output offsets [NB], kept blocks per request [R]
+  off = align256(off + sizeof(int32_t) * (2 * size_t(pl->NB) + size_t(pl->R)));
   pl->total = off;
   pl->nonempty = 0;
   for (int r = 0; r < pl->R; ++r) pl->nonempty += b->cu_seqlens_host[r + 1] > b->cu_seqlens_host[r];
@@ -524,14 +527,17 @@ upf::DescribeArgs describe_args(const upf_ctx* ctx, const upf_batch* b, const Pl
   return a;
 }
 
-// Arguments of the fused tail; kept_list / cu_out / total_kept nullable.
-upf::TailArgs tail_args(const upf::SelectArgs& se, const Plan& pl, void* ws, int32_t* kept_list, int32_t* cu_out,
+// Arguments of the fused tail; with_lists: the kept-block lists for the
+// gather; cu_out / total_kept nullable.
+upf::TailArgs tail_args(const upf::SelectArgs& se, const Plan& pl, void* ws, bool with_lists, int32_t* cu_out,
                         int32_t* total_kept) {
   upf::TailArgs t;
   t.s = se;
   t.counters = at<int32_t>(ws, pl.off_ctr);
   t.edge_bits = reinterpret_cast<uint32_t*>(t.counters + (pl.R + 1));
-  t.kept_list = kept_list;
+  t.kept_blk = with_lists ? at<int32_t>(ws, pl.off_kbl) : nullptr;
+  t.kept_off = with_lists ? t.kept_blk + pl.NB : nullptr;
+  t.kept_nblk = with_lists ? t.kept_blk + 2 * pl.NB : nullptr;
   t.cu_out = cu_out;
   t.total_kept = total_kept;
   t.nonempty = pl.nonempty;
@@ -854,7 +860,7 @@ upf_status upf_select(upf_ctx* ctx, const upf_batch* batch, const upf_params* pa
   upf::SelectArgs se = select_args(ctx, batch, pl, ws, 0, nullptr, scores, nullptr, block_scores, keep_bits,
                                    kept_count);
   if (fused_tail(pl)) {
-    const upf::TailArgs ta = tail_args(se, pl, ws, nullptr, nullptr, nullptr);
+    const upf::TailArgs ta = tail_args(se, pl, ws, false, nullptr, nullptr);
     UPF_LAUNCH(staged(ctx, kSelect, s, [&] { return upf::launch_tail(ta, s, true); }), "block means and select");
     return UPF_OK;
   }
@@ -939,15 +945,19 @@ upf_status upf_select_tokens(upf_ctx* ctx, const upf_batch* batch, const upf_par
   upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC * pl.pw, sa.part, nullptr, scores, block_scores,
                                    keep_bits, kept_count);
   if (fused_tail(pl)) {
-    // finalize + block means + select + kept-token list + compacted offsets in
-    // one launch, then the gather driven by the per-request lists
-    int32_t* kept_list = at<int32_t>(ws, pl.off_kidx);
-    const upf::TailArgs ta = tail_args(se, pl, ws, kept_list, io->cu_seqlens_out, io->total_kept);
+    // finalize + block means + select + kept-block lists + compacted offsets
+    // in one launch, then the gather driven by the kept-block lists
+    const upf::TailArgs ta = tail_args(se, pl, ws, true, io->cu_seqlens_out, io->total_kept);
     UPF_LAUNCH(staged(ctx, kSelect, s, [&] { return upf::launch_tail(ta, s, true); }), "finalize and select");
-    upf::CompactArgs ca = compact_args(ctx, batch, pl, keep_bits, io, ws);
-    ca.kept_index = io->kept_index;   // the workspace's index area holds the lists
-    UPF_LAUNCH(staged(ctx, kCompactGather, s, [&] { return upf::launch_gather_list(ca, kept_list, s, true); }),
-               "compact gather");
+    upf::GatherListArgs ga;
+    ga.c = compact_args(ctx, batch, pl, keep_bits, io, ws);
+    ga.c.kept_index = io->kept_index;   // nullable: written only if the caller asks
+    ga.blk_off = se.blk_off;
+    ga.kept_blk = ta.kept_blk;
+    ga.kept_off = ta.kept_off;
+    ga.kept_nblk = ta.kept_nblk;
+    ga.G = pl.G;
+    UPF_LAUNCH(staged(ctx, kCompactGather, s, [&] { return upf::launch_gather_list(ga, s, true); }), "compact gather");
     return UPF_OK;
   }
   UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s, true); }), "finalize scores");

@@ -98,7 +98,9 @@ struct TailArgs {
   SelectArgs s;
   int32_t* counters;    // [R+1], zero on entry: CTAs done per request, then requests done
   uint32_t* edge_bits;  // [2R] keep bits of each request's first and last word when shared
-  int32_t* kept_list;   // [T] (nullable): request r's kept tokens at [cu[r], cu[r] + kept_r)
+  int32_t* kept_blk;    // [NB] (nullable): request r's kept blocks, in order, at blk_off[r] + m
+  int32_t* kept_off;    // [NB]: output offset (within the request) of each of those blocks
+  int32_t* kept_nblk;   // [R]: kept blocks per request
   int32_t* cu_out;      // [R+1] (nullable, then total_kept too)
   int32_t* total_kept;  // [1]
   int32_t nonempty;     // requests with at least one token (host value)
@@ -198,7 +200,16 @@ cudaError_t launch_compact_gather(const CompactArgs& a, cudaStream_t s, bool pdl
 int tail_blocks_per_cta(int G);
 size_t tail_smem_bytes(int G, int max_nb);
 cudaError_t launch_tail(const TailArgs& a, cudaStream_t s, bool pdl = false);
-cudaError_t launch_gather_list(const CompactArgs& a, const int32_t* kept_list, cudaStream_t s, bool pdl = false);
+// The gather of the fused path, driven by the tail kernel's kept-block lists.
+struct GatherListArgs {
+  CompactArgs c;
+  const int32_t* blk_off;   // [R+1]
+  const int32_t* kept_blk;
+  const int32_t* kept_off;
+  const int32_t* kept_nblk;
+  int32_t G;
+};
+cudaError_t launch_gather_list(const GatherListArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_revive(const ReviveArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_history_kv_len(const HistoryArgs& a, cudaStream_t s, bool pdl = false);
 
