@@ -99,15 +99,20 @@ __device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity, lo
   return true;
 }
 
-// mbar_wait_idle that also gives up (false) once *abort becomes non-zero; the
-// flag is read only while the phase is pending, so an uncontended wait costs
-// nothing extra.
+// mbar_wait_idle that also gives up (false) once *abort is non-zero.  The
+// flag is read only after the wait has lasted kAbortPollCycles (about 32 us,
+// far longer than any wait of a working pipeline): a shared-memory load in
+// every poll would compete with the loads of busy warps on the same
+// scheduler.
+constexpr long long kAbortPollCycles = 1LL << 16;
 __device__ __forceinline__ bool mbar_wait_idle_abortable(uint32_t bar, uint32_t parity, long long limit, uint32_t ns,
                                                          const int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait_hint(bar, parity, ns)) {
-    if (*reinterpret_cast<const volatile int*>(abort) != 0 || clock64() - t0 > limit) return false;
+    const long long dt = clock64() - t0;
+    if (dt > limit) return false;
+    if (dt > kAbortPollCycles && *reinterpret_cast<const volatile int*>(abort) != 0) return false;
   }
   return true;
 }

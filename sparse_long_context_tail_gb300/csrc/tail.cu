@@ -313,13 +313,22 @@ __global__ void __launch_bounds__(256) gather_list_kernel(const GatherListArgs g
     const int r = owner_of(a.cu_out, a.R, o);
     const int j = o - a.cu_out[r];
     const int base = g.blk_off[r];
-    int lo = 0, hi = g.kept_nblk[r] - 1;
-    if (hi < 0) continue;   // never for a consistent batch
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (g.kept_off[base + mid] <= j) lo = mid;
-      else hi = mid - 1;
+    // 32-way search: each lane probes one of 32 evenly spaced kept blocks and
+    // the last probe at or below j narrows the range (one round for up to 32
+    // kept blocks, two for up to 1024).
+    int lo = 0, n = g.kept_nblk[r];
+    if (n <= 0) continue;   // never for a consistent batch
+    while (n > 1) {
+      const int step = (n + 31) >> 5;
+      const int at = lane * step;
+      const bool le = at < n && g.kept_off[base + lo + at] <= j;
+      const unsigned below = __ballot_sync(0xffffffffu, le);   // lane 0 always: offset 0 <= j
+      if (!below) break;   // never for a consistent batch
+      const int last = 31 - __clz(below);
+      lo += last * step;
+      n = min(step, n - last * step);
     }
+    if (n != 1) continue;
     const int t = a.cu[r] + g.kept_blk[base + lo] * g.G + (j - g.kept_off[base + lo]);
     if (t < a.cu[r] || t >= a.cu[r + 1] || t >= a.T) continue;   // never for a consistent batch
     if (lane == 0 && a.kept_index) a.kept_index[o] = t;
