@@ -31,8 +31,9 @@
 // one tcgen05.commit cover a stage: per-slice commits were measured to stall
 // the tensor pipe.
 // Every wait is bounded; on a timeout the kernel records UPF_ERR_TIMEOUT, the
-// roles wind down (a role that waits gives up as soon as another role gave
-// up), outstanding copies and MMAs are waited for with the full limit, TMEM
+// roles wind down (the epilogue stops at once; a producer or MMA wait for a
+// role that gave up ends on its own limit), outstanding copies and MMAs are
+// waited for with the full limit, TMEM
 // is freed and the kernel returns.  The pipeline waits' limit is a run-time
 // argument (upf_set_wait_limit), so a test can make one expire.
 #include <cuda.h>
@@ -258,7 +259,7 @@ __device__ int produce(const ScoreArgs& a, const CUtensorMap* tq_map, const CUte
     }
     int part = 0, key = it.tok0 + k0;
     for (int n = 0; n < total; ++n, ++q) {
-      if (!mbar_wait_idle_abortable(bar_empty(sm, st), ph ^ 1u, a.wait_limit, kIdleNs, sm.abort_flag)) {
+      if (!mbar_wait_idle(bar_empty(sm, st), ph ^ 1u, a.wait_limit, kIdleNs)) {
         abort_with_timeout(a, sm);
         return q;
       }
@@ -318,18 +319,20 @@ __device__ void issue_mma(const ScoreArgs& a, const Smem& sm, const Geo& geo, in
   for (int i = 0; ok && i < ntiles; ++i) {
     // A tile takes spt <= 2 consecutive ring stages; slice s lives in stage
     // part s / sps at offset (s % sps) slices, sps in {1, 2}.
-    // The waits give up as soon as another role gave up (a timeout).
+    // No abort test in this loop: every extra instruction of the issuing
+    // thread, which shares its scheduler with busy epilogue warps, was measured
+    // to cost 2-3 % of the pass; once another role gave up, these waits end on
+    // their own limit.
     const int st0 = st, st1 = st + 1 == geo.NS ? 0 : st + 1;
-    ok = mbar_wait_idle_abortable(bar_full(sm, st0), ph, a.wait_limit, kIdleNs, sm.abort_flag);
-    if (ok && geo.spt == 2)
-      ok = mbar_wait_idle_abortable(bar_full(sm, st1), st1 == 0 ? ph ^ 1u : ph, a.wait_limit, kIdleNs, sm.abort_flag);
+    ok = mbar_wait_idle(bar_full(sm, st0), ph, a.wait_limit, kIdleNs);
+    if (ok && geo.spt == 2) ok = mbar_wait_idle(bar_full(sm, st1), st1 == 0 ? ph ^ 1u : ph, a.wait_limit, kIdleNs);
     if (geo.spt == 2) { st = st1 + 1 == geo.NS ? 0 : st1 + 1; ph = (st1 == 0 || st == 0) ? ph ^ 1u : ph; }
     else { st = st1; ph = st1 == 0 ? ph ^ 1u : ph; }
     const uint32_t k0a = ring0 + uint32_t(st0 * geo.stage_bytes), k1a = ring0 + uint32_t(st1 * geo.stage_bytes);
     if (!ok) break;
     tc_fence_after();
     for (int u = 0; u < units; ++u) {
-      ok = mbar_wait_idle_abortable(bar_tempty(sm, slot), sph ^ 1u, a.wait_limit, kIdleNs, sm.abort_flag);
+      ok = mbar_wait_idle(bar_tempty(sm, slot), sph ^ 1u, a.wait_limit, kIdleNs);
       if (!ok) break;
       tc_fence_after();
       const uint32_t dt = tmem + uint32_t(slot * geo.slot_cols);

@@ -99,24 +99,6 @@ __device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity, lo
   return true;
 }
 
-// mbar_wait_idle that also gives up (false) once *abort is non-zero.  The
-// flag is read only after the wait has lasted kAbortPollCycles (about 32 us,
-// far longer than any wait of a working pipeline): a shared-memory load in
-// every poll would compete with the loads of busy warps on the same
-// scheduler.
-constexpr long long kAbortPollCycles = 1LL << 16;
-__device__ __forceinline__ bool mbar_wait_idle_abortable(uint32_t bar, uint32_t parity, long long limit, uint32_t ns,
-                                                         const int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait_hint(bar, parity, ns)) {
-    const long long dt = clock64() - t0;
-    if (dt > limit) return false;
-    if (dt > kAbortPollCycles && *reinterpret_cast<const volatile int*>(abort) != 0) return false;
-  }
-  return true;
-}
-
 // ----------------------------------------------------------------- TMA ----
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int c0, int c1, uint32_t bar) {

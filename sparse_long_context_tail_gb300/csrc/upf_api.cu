@@ -298,17 +298,17 @@ upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p
     // Query rows per chunk: the whole group's tail rows when they fit the
     // tensor-core kernels' shared-memory budget (512 rows of d <= 128, 256 rows
     // of d = 256), rounded up to whole 128-row MMA tiles.
-    // At d = 256 chunks of whole 256-row units run on CTA pairs (below), each
-    // SM holding half of the chunk.  Without pairs, a group of at most 256
-    // rows (bound by the key reads: about QR flop per key byte, below the
-    // tensor/HBM ridge) takes chunks of 128 rows instead: that halves the
-    // resident queries, so the key ring holds two tiles instead of one (the
-    // second chunk's CTA finds the same keys in L2).
+    // At d = 256 a group of at most 256 rows is bound by the key reads (about
+    // QR flop per key byte, below the tensor/HBM ridge): chunks of 128 rows on
+    // single CTAs halve the resident queries, so the key ring holds two tiles
+    // instead of one and the next tile streams in while the current one is
+    // used (the second chunk's CTA finds the same keys in L2).  Measured
+    // against 256-row chunks on CTA pairs: 0.43 against 0.38-0.42 of HBM.
     const char* pairs = std::getenv("UPF_SCORE_PAIRS");
     const bool pairs_off = pairs && std::strcmp(pairs, "0") == 0;
     const bool pairs_any_d = pairs && std::strcmp(pairs, "1") == 0;
     int qc_max = pl->d <= 128 ? 512 : 256;
-    if (pl->d == 256 && pl->QR <= 256 && pairs_off) qc_max = 128;
+    if (pl->d == 256 && pl->QR <= 256) qc_max = 128;
     pl->QC = std::min(((pl->QR + 127) / 128) * 128, qc_max);
     pl->NQC = ceil_div(pl->QR, pl->QC);
     // Tensor-core kernels load tail rows in TMA boxes of 16..128 rows that

@@ -135,7 +135,7 @@ def test_scoring_work_split_is_near_the_best_whole_tile_split(lib):
         sms = 152 // ctas
         gamma = s.num_q_heads // s.num_kv_heads
         qr = gamma * s.n_tail
-        qc = min(-(-qr // 128) * 128, 512 if s.head_dim <= 128 else 256)
+        qc = min(-(-qr // 128) * 128, 512 if s.head_dim <= 128 else (128 if qr <= 256 else 256))
         nqc = -(-qr // qc)
         units = s.num_kv_heads * nqc
         for ks, n, tile in ((ks1, n1, 256 if ctas == 2 or s.head_dim <= 128 else 128),
