@@ -38,10 +38,15 @@ DEFAULT_WORKLOAD = "llama8b-L131072"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 STAGES = ["describe", "score_pass1", "score_pass2", "finalize", "select", "compact_count", "compact_index",
           "compact_gather"]
-# kernel sources per stage (for the traffic record's freshness check)
-STAGE_SOURCES = {"score_pass1": "score_tc.cu", "score_pass2": "score_tc.cu", "finalize": "select.cu",
-                 "select": "select.cu", "compact_gather": "compact.cu", "compact_index": "compact.cu",
-                 "compact_count": "compact.cu", "describe": "score_simt.cu"}
+# kernel sources per stage (for the traffic record's freshness check): the
+# translation unit of the kernel the fused call launches plus the headers it
+# includes from the package
+_TC = ["score_tc.cu", "score_common.cuh", "sm100_ptx.cuh", "upf_internal.cuh"]
+_TAIL = ["tail.cu", "select_core.cuh", "upf_internal.cuh"]
+STAGE_SOURCES = {"score_pass1": _TC, "score_pass2": _TC, "finalize": _TAIL, "select": _TAIL,
+                 "compact_gather": _TAIL, "compact_index": ["compact.cu", "upf_internal.cuh"],
+                 "compact_count": ["compact.cu", "upf_internal.cuh"],
+                 "describe": ["score_simt.cu", "upf_internal.cuh"]}
 
 
 def log(*a):
@@ -110,11 +115,18 @@ def load_peaks():
 
 
 def source_sha(stage):
-    src = os.path.join(ROOT, "sparse_long_context_tail_gb300", "csrc", STAGE_SOURCES.get(stage, ""))
-    if not os.path.isfile(src):
+    """First 16 hex digits of the SHA-256 of the stage's sources, concatenated."""
+    files = STAGE_SOURCES.get(stage)
+    if not files:
         return None
-    with open(src, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in files:
+        src = os.path.join(ROOT, "sparse_long_context_tail_gb300", "csrc", name)
+        if not os.path.isfile(src):
+            return None
+        with open(src, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def traffic_record(stage, workload):
@@ -126,7 +138,8 @@ def traffic_record(stage, workload):
         with open(p) as f:
             rec = json.load(f)
         r = rec.get(stage)
-        if r and r.get("workload") == workload and r.get("source_sha") == source_sha(stage):
+        sha = source_sha(stage)
+        if r and sha is not None and r.get("workload") == workload and r.get("source_sha") == sha:
             return float(r["dram_bytes_per_launch"])
     except (OSError, ValueError, KeyError):
         return None

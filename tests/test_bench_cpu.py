@@ -42,15 +42,23 @@ def test_algorithmic_work_of_requests_shorter_than_the_tail():
 def test_traffic_record_is_dropped_once_the_kernel_changes(tmp_path, monkeypatch):
     src = tmp_path / "sparse_long_context_tail_gb300" / "csrc"
     src.mkdir(parents=True)
-    (src / "score_tc.cu").write_text("// version 1\n")
+    files = bench.STAGE_SOURCES["score_pass1"]
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    sha = bench.source_sha("score_pass1")
     (tmp_path / "profiles").mkdir()
+    for name in files[:-1]:
+        (src / name).write_text(f"// {name} version 1\n")
+    assert bench.source_sha("score_pass1") is None          # a source missing: never current
+    (src / files[-1]).write_text("// header version 1\n")
+    sha = bench.source_sha("score_pass1")
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(
         {"score_pass1": {"workload": "w", "source_sha": sha, "dram_bytes_per_launch": 1234}}))
     assert bench.traffic_record("score_pass1", "w") == 1234.0
     assert bench.traffic_record("score_pass1", "another workload") is None
-    (src / "score_tc.cu").write_text("// version 2\n")
+    (src / files[-1]).write_text("// header version 2\n")   # an included header changed
+    assert bench.traffic_record("score_pass1", "w") is None
+    (src / files[-1]).write_text("// header version 1\n")
+    assert bench.traffic_record("score_pass1", "w") == 1234.0
+    (src / files[0]).write_text("// kernel version 2\n")
     assert bench.traffic_record("score_pass1", "w") is None
 
 
