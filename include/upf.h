@@ -64,7 +64,13 @@ typedef struct upf_ctx upf_ctx;
 /* Batch descriptor (section 三: continuous batching; GQA head layout).
  * cu_seqlens_dev:  device int32 [num_reqs+1], cu[0] = 0, non-decreasing.
  * cu_seqlens_host: host copy of the same values (used to size grids and the
- *                  workspace; the device copy is re-checked on the GPU).
+ *                  workspace; the device copy is re-checked on the GPU, and a
+ *                  disagreement is reported through the status word as
+ *                  UPF_ERR_INVALID_ARG).  upf_select_tokens on the tensor-core
+ *                  path with at most 64 requests addresses the batch through
+ *                  the host copy (its descriptor travels in the kernel
+ *                  parameters); otherwise the device copy, once checked,
+ *                  drives the kernels and a rejected one makes them do no work.
  * num_q_heads, num_kv_heads: H_q and H_kv, H_q % H_kv == 0.
  * head_dim: d, one of 64, 128, 256.
  * kv_of_q: host int32 [H_q] giving the kv head each q head reads, every kv head
@@ -320,8 +326,10 @@ upf_status upf_select_noalloc(const upf_batch* batch, const upf_params* params, 
 upf_status upf_set_wait_limit(upf_ctx* ctx, int64_t cycles);
 
 /* Tracing (per-stage device timing).  Stages, in launch order:
- * 0 describe (batch descriptor), 1 score pass 1, 2 score pass 2, 3 finalize /
- * block means, 4 select, 5 compact count, 6 compact index, 7 compact gather. */
+ * 0 describe (batch descriptor; upf_select_tokens launches none for batches
+ * whose descriptor travels in the kernel parameters), 1 score pass 1, 2 score
+ * pass 2, 3 finalize / block means, 4 select, 5 compact count, 6 compact
+ * index, 7 compact gather. */
 #define UPF_NUM_STAGES 8
 
 /* Name of stage i (static string; "" if out of range). */

@@ -61,6 +61,39 @@ __device__ __forceinline__ int64_t item_index(const int32_t* item_off, int r, in
   return item_off[r] + ((int64_t)g * nsplit + s) * NQC + qc;
 }
 
+// Work item `item` of pass 1 (pass2 false) or pass 2 and the first pass-1
+// item of a row group, from the tables carried in the parameters (a must be
+// the kernel's __grid_constant__ parameter) or else the workspace tables
+// describe_kernel wrote.  Each branch reads its own tables directly: a pointer
+// chosen at run time between the two spaces costs the epilogue warps
+// registers they do not have (measured: spills in both passes).
+__device__ __forceinline__ bool item_exists(const ScoreArgs& a, int item, bool pass2) {
+  if (item >= (pass2 ? a.items2 : a.items1)) return false;
+  if (a.desc.R > 0) return item < (pass2 ? a.desc.off2[a.R] : a.desc.off1[a.R]);
+  return item < (pass2 ? a.item_off2[a.R] : a.item_off1[a.R]);
+}
+__device__ __forceinline__ ItemTC locate_item(const ScoreArgs& a, int item, bool pass2) {
+  if (a.desc.R > 0) return locate_tc(pass2 ? a.desc.off2 : a.desc.off1, a.desc.cu, a.R, item, pass2 ? a.KS2 : a.KS1, a.NQC);
+  return locate_tc(pass2 ? a.item_off2 : a.item_off1, a.cu, a.R, item, pass2 ? a.KS2 : a.KS1, a.NQC);
+}
+__device__ __forceinline__ int64_t pass1_item_index(const ScoreArgs& a, int r, int g, int qc, int nsplit1) {
+  if (a.desc.R > 0) return item_index(a.desc.off1, r, g, 0, qc, nsplit1, a.NQC);
+  return item_index(a.item_off1, r, g, 0, qc, nsplit1, a.NQC);
+}
+
+// With carried tables, one warp of pass 1's first CTA does what
+// describe_kernel does otherwise: it checks the device cu_seqlens against the
+// host's (a disagreement is reported; every kernel addresses the batch through
+// the carried tables, so it cannot move any work out of bounds) and clears
+// the tail kernel's counters, which run only after pass 2 has finished.
+__device__ __forceinline__ void desc_check(const ScoreArgs& a, int lane) {
+  if (a.desc.R <= 0) return;
+  bool bad = false;
+  for (int i = lane; i <= a.desc.R; i += 32) bad |= a.cu[i] != a.desc.cu[i];
+  for (int i = lane; i < a.ncounters; i += 32) a.counters[i] = 0;
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(a.status, UPF_ERR_INVALID_ARG);
+}
+
 // ------------------------------------------------------- epilogue math -----
 
 // sum_j 2^(v[j] * sl - ref) over 32 values, with the affine step and the

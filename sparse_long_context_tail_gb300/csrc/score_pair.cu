@@ -259,6 +259,7 @@ __device__ void pair_relay(const ScoreArgs& a, const PSmem& sm, const PGeo& geo,
 
 // CTA 0's MMA thread.  keys_as_m: pass 2 (A = key stage, B = query unit);
 // else pass 1 (A = query unit, B = key stage).
+template <bool kEarly>
 __device__ void pair_mma(const ScoreArgs& a, const PSmem& sm, const PGeo& geo, int ntiles, int U, uint32_t tmem,
                          bool keys_as_m) {
   const uint32_t idesc = idesc_bf16_f32(256, 256);
@@ -274,11 +275,17 @@ __device__ void pair_mma(const ScoreArgs& a, const PSmem& sm, const PGeo& geo, i
       ok = false;
       break;
     }
+    // Pass 2 (kEarly) with two stages per tile: the tile's first unit starts
+    // on the first stage while the second may still be landing, and the first
+    // stage is released as soon as the last unit has read it (as in the
+    // single-CTA kernels).  Measured faster in pass 2 and slower in pass 1,
+    // where the release is a commit in the middle of the tile's only unit.
     const int st0 = st, st1 = st + 1 == geo.NS ? 0 : st + 1;
     const uint32_t ph1 = st1 == 0 ? ph ^ 1u : ph;
+    const bool two = kEarly && geo.spt == 2;
     ok = mbar_wait_idle(b_full(sm, st0), ph, a.wait_limit, kIdleNs) &&
          mbar_wait_cluster(b_pfull(sm, st0), ph, a.wait_limit, kRemoteNs);
-    if (ok && geo.spt == 2)
+    if (!kEarly && ok && geo.spt == 2)
       ok = mbar_wait_idle(b_full(sm, st1), ph1, a.wait_limit, kIdleNs) &&
            mbar_wait_cluster(b_pfull(sm, st1), ph1, a.wait_limit, kRemoteNs);
     if (geo.spt == 2) { st = st1 + 1 == geo.NS ? 0 : st1 + 1; ph = (st1 == 0 || st == 0) ? ph ^ 1u : ph; }
@@ -293,6 +300,15 @@ __device__ void pair_mma(const ScoreArgs& a, const PSmem& sm, const PGeo& geo, i
       const uint32_t dt = tmem + uint32_t(slot * 256);
       const uint32_t qu = q0 + uint32_t(u) * q_unit;
       for (int s = 0; s < geo.S; ++s) {
+        if (kEarly && two && s == geo.sps) {   // the first slice of the second stage
+          if (u == U - 1) mma_commit_pair_mc(b_empty(sm, st0), 0x3);
+          if (u == 0) {
+            ok = mbar_wait_idle(b_full(sm, st1), ph1, a.wait_limit, kIdleNs) &&
+                 mbar_wait_cluster(b_pfull(sm, st1), ph1, a.wait_limit, kRemoteNs);
+            if (!ok) break;
+            tc_fence_after();
+          }
+        }
         const int part = geo.sps == 2 ? (s >> 1) : s;
         const uint32_t kb = (part == 0 ? k0a : k1a) + uint32_t(geo.sps == 2 ? (s & 1) * geo.slice_bytes : 0);
         const uint32_t qb = qu + uint32_t(s) * q_slice;
@@ -302,12 +318,17 @@ __device__ void pair_mma(const ScoreArgs& a, const PSmem& sm, const PGeo& geo, i
         for (int kk = 0; kk < 4; ++kk)   // +32 bytes along K = +2 in the descriptors' address field
           mma_bf16_pair(dt, da + uint64_t(2 * kk), db + uint64_t(2 * kk), idesc, (s | kk) ? 1u : 0u);
       }
+      if (kEarly && !ok) break;
       mma_commit_pair_mc(b_tfull(sm, slot), 0x3);
       if (++slot == kSlots) { slot = 0; sph ^= 1u; }
     }
     if (!ok) break;
-    mma_commit_pair_mc(b_empty(sm, st0), 0x3);
-    if (geo.spt == 2) mma_commit_pair_mc(b_empty(sm, st1), 0x3);
+    if (!kEarly) {
+      mma_commit_pair_mc(b_empty(sm, st0), 0x3);
+      if (geo.spt == 2) mma_commit_pair_mc(b_empty(sm, st1), 0x3);
+    } else {
+      mma_commit_pair_mc(b_empty(sm, two ? st1 : st0), 0x3);
+    }
   }
   if (!ok) pabort(a, sm, 0);
   // Every MMA issued must be done before either CTA frees TMEM (full limit).
@@ -452,10 +473,10 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   extern __shared__ unsigned char smem_raw[];
   const int item = blockIdx.x >> 1;
   const uint32_t rank = cluster_ctarank();
-  if (item >= a.items1 || item >= a.item_off1[a.R]) return;   // both CTAs of the pair alike
+  if (!item_exists(a, item, false)) return;   // both CTAs of the pair alike
   const PGeo geo = pair_geometry(1, a.d, a.QC);
   const PSmem sm = pcarve(smem_raw, geo, a.QC);
-  const ItemTC it = locate_tc(a.item_off1, a.cu, a.R, item, a.KS1, a.NQC);
+  const ItemTC it = locate_item(a, item, false);
   const int rows_c = chunk_rows_p(a, it.qc);
   const int U = (rows_c + 255) / 256;
   const int k0 = it.s * a.KS1, k1 = min(it.L, k0 + a.KS1);
@@ -465,9 +486,10 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   int issued = 0;
   if (warp == kProducerWarp) {
     if (lane == 0) issued = pair_produce(a, &tq_map, &tk_map, sm, geo, it, rows_c, U, k0, ntiles, rank);
+    if (blockIdx.x == 0) desc_check(a, lane);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      if (rank == 0) pair_mma(a, sm, geo, ntiles, U, tmem, false);
+      if (rank == 0) pair_mma<false>(a, sm, geo, ntiles, U, tmem, false);
       else pair_relay(a, sm, geo, ntiles);
     }
   } else {
@@ -561,10 +583,10 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   extern __shared__ unsigned char smem_raw[];
   const int item = blockIdx.x >> 1;
   const uint32_t rank = cluster_ctarank();
-  if (item >= a.items2 || item >= a.item_off2[a.R]) return;   // both CTAs of the pair alike
+  if (!item_exists(a, item, true)) return;   // both CTAs of the pair alike
   const PGeo geo = pair_geometry(2, a.d, a.QC);
   const PSmem sm = pcarve(smem_raw, geo, a.QC);
-  const ItemTC it = locate_tc(a.item_off2, a.cu, a.R, item, a.KS2, a.NQC);
+  const ItemTC it = locate_item(a, item, true);
   const int rows_c = chunk_rows_p(a, it.qc);
   const int U = (rows_c + 255) / 256;
   const int qcols = U * 256;
@@ -577,7 +599,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
     if (lane == 0) issued = pair_produce(a, &tq_map, &tk_map, sm, geo, it, rows_c, U, k0, ntiles, rank);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      if (rank == 0) pair_mma(a, sm, geo, ntiles, U, tmem, true);
+      if (rank == 0) pair_mma<true>(a, sm, geo, ntiles, U, tmem, true);
       else pair_relay(a, sm, geo, ntiles);
     }
   } else {
@@ -590,7 +612,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       int t = -1;
       if (row < rows_c) {
         t = it.L - a.n + (it.qc * a.QC + row) % a.n;
-        const float2* src = a.p1part + item_index(a.item_off1, it.r, it.g, 0, it.qc, nsplit1, a.NQC) * a.QC + row;
+        const float2* src = a.p1part + pass1_item_index(a, it.r, it.g, it.qc, nsplit1) * a.QC + row;
         const int64_t split_stride = (int64_t)a.NQC * a.QC;
         float mm = -INFINITY, Z = 0.f;
         for (int s0 = 0; s0 < nsplit1; s0 += 16) {

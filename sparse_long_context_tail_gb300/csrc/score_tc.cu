@@ -297,6 +297,7 @@ __device__ void drain_loads(const Smem& sm, const Geo& geo, int issued) {
 // that issues it).  Measured on the 128K-token LLaMA shape, the warp-wide
 // form makes pass 1 about 3 % faster and pass 2 about 3 % slower, so pass 2
 // keeps one lane.
+template <bool kEarly>
 __device__ void issue_mma(const ScoreArgs& a, const Smem& sm, const Geo& geo, int ntiles, int units, uint32_t tmem,
                           bool keys_as_m, bool may_repeat, bool warp_wide) {
   const bool leader = warp_wide ? elect_one() : true;
@@ -323,9 +324,19 @@ __device__ void issue_mma(const ScoreArgs& a, const Smem& sm, const Geo& geo, in
     // thread, which shares its scheduler with busy epilogue warps, was measured
     // to cost 2-3 % of the pass; once another role gave up, these waits end on
     // their own limit.
+    // With two stages per tile (kEarly), the tile's first unit starts on the
+    // first stage while the second may still be landing, and the first stage
+    // is released as soon as the last unit has read it: the next tile's second
+    // load then has about two units of MMA work to arrive behind, not none.
+    // Measured faster in pass 1 and in pass 2 with two or more units per tile;
+    // with one unit per tile the pass-2 release is a commit in the middle of a
+    // unit, which stalls the tensor pipe more than the earlier load gains.  A
+    // compile-time choice: even the untaken tests cost this thread's loop time.
     const int st0 = st, st1 = st + 1 == geo.NS ? 0 : st + 1;
+    const uint32_t ph1 = st1 == 0 ? ph ^ 1u : ph;
+    const bool two = kEarly && geo.spt == 2;
     ok = mbar_wait_idle(bar_full(sm, st0), ph, a.wait_limit, kIdleNs);
-    if (ok && geo.spt == 2) ok = mbar_wait_idle(bar_full(sm, st1), st1 == 0 ? ph ^ 1u : ph, a.wait_limit, kIdleNs);
+    if (!kEarly && ok && geo.spt == 2) ok = mbar_wait_idle(bar_full(sm, st1), ph1, a.wait_limit, kIdleNs);
     if (geo.spt == 2) { st = st1 + 1 == geo.NS ? 0 : st1 + 1; ph = (st1 == 0 || st == 0) ? ph ^ 1u : ph; }
     else { st = st1; ph = st1 == 0 ? ph ^ 1u : ph; }
     const uint32_t k0a = ring0 + uint32_t(st0 * geo.stage_bytes), k1a = ring0 + uint32_t(st1 * geo.stage_bytes);
@@ -338,6 +349,14 @@ __device__ void issue_mma(const ScoreArgs& a, const Smem& sm, const Geo& geo, in
       const uint32_t dt = tmem + uint32_t(slot * geo.slot_cols);
       const uint32_t qu = q0 + uint32_t(u) * q_unit;
       for (int s = 0; s < geo.S; ++s) {
+        if (kEarly && two && s == geo.sps) {   // the first slice of the second stage
+          if (u == units - 1 && leader) mma_commit(bar_empty(sm, st0));
+          if (u == 0) {
+            ok = mbar_wait_idle(bar_full(sm, st1), ph1, a.wait_limit, kIdleNs);
+            if (!ok) break;
+            tc_fence_after();
+          }
+        }
         const int part = geo.sps == 2 ? (s >> 1) : s;
         const uint32_t kb = (part == 0 ? k0a : k1a) + uint32_t(geo.sps == 2 ? (s & 1) * geo.slice_bytes : 0);
         const uint32_t qb = qu + uint32_t(s) * q_slice;
@@ -347,13 +366,18 @@ __device__ void issue_mma(const ScoreArgs& a, const Smem& sm, const Geo& geo, in
         for (int kk = 0; kk < 4; ++kk)   // +32 bytes along K = +2 in the descriptors' address field
           if (leader) mma_bf16(dt, da + uint64_t(2 * kk), db + uint64_t(2 * kk), idesc, (s | kk) ? 1u : 0u);
       }
+      if (kEarly && !ok) break;
       if (leader) mma_commit(bar_tfull(sm, slot));
       if (++slot == geo.nslots) { slot = 0; sph ^= 1u; }
     }
     if (!ok) break;
     if (leader) {
-      mma_commit(bar_empty(sm, st0));
-      if (geo.spt == 2) mma_commit(bar_empty(sm, st1));
+      if (!kEarly) {
+        mma_commit(bar_empty(sm, st0));
+        if (geo.spt == 2) mma_commit(bar_empty(sm, st1));
+      } else {
+        mma_commit(bar_empty(sm, two ? st1 : st0));
+      }
     }
   }
   }
@@ -558,10 +582,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   pdl_wait();
   extern __shared__ unsigned char smem_raw[];
   const int item = blockIdx.x;
-  if (item >= a.items1 || item >= a.item_off1[a.R]) return;
+  if (!item_exists(a, item, false)) return;
   const Geo geo = geometry(1, a.d, a.QC);
   const Smem sm = carve(smem_raw, geo, a.QC);
-  const ItemTC it = locate_tc(a.item_off1, a.cu, a.R, item, a.KS1, a.NQC);
+  const ItemTC it = locate_item(a, item, false);
   const int rows_c = chunk_rows(a, it.qc);
   const int k0 = it.s * a.KS1, k1 = min(it.L, k0 + a.KS1);
   const int ntiles = ceil_div_dev(k1 - k0, geo.tile_keys);
@@ -572,8 +596,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   int issued = 0;
   if (warp == kProducerWarp) {
     issued = produce(a, &tq_map, &tk_map, sm, geo, it, rows_c, k0, ntiles, true, true);
+    if (blockIdx.x == 0) desc_check(a, lane);
   } else if (warp == kMmaWarp) {
-    issue_mma(a, sm, geo, ntiles, MT, tmem, false, true, true);
+    issue_mma<true>(a, sm, geo, ntiles, MT, tmem, false, true, true);
   } else if (geo.tile_keys / kW == 64) {
     pass1_epilogue<2>(a, sm, geo, it, item, rows_c, MT, k0, ntiles, tmem, warp, lane);
   } else {
@@ -666,10 +691,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   pdl_wait();
   extern __shared__ unsigned char smem_raw[];
   const int item = blockIdx.x;
-  if (item >= a.items2 || item >= a.item_off2[a.R]) return;
+  if (!item_exists(a, item, true)) return;
   const Geo geo = geometry(2, a.d, a.QC);
   const Smem sm = carve(smem_raw, geo, a.QC);
-  const ItemTC it = locate_tc(a.item_off2, a.cu, a.R, item, a.KS2, a.NQC);
+  const ItemTC it = locate_item(a, item, true);
   const int rows_c = chunk_rows(a, it.qc);
   const int U = (rows_c + geo.unit_cols - 1) / geo.unit_cols;   // units per tile
   const int qcols = U * geo.unit_cols;                         // MMA columns (zero-padded query rows)
@@ -682,7 +707,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   if (warp == kProducerWarp) {
     if (lane == 0) issued = produce(a, &tq_map, &tk_map, sm, geo, it, rows_c, k0, ntiles, false, false);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) issue_mma(a, sm, geo, ntiles, U, tmem, true, false, false);
+    if (lane == 0) {
+      if (U >= 2) issue_mma<true>(a, sm, geo, ntiles, U, tmem, true, false, false);
+      else issue_mma<false>(a, sm, geo, ntiles, U, tmem, true, false, false);
+    }
   } else {
     // lse2 of every query row of the chunk from the pass-1 partials (all key
     // splits), stored negated; -inf marks rows that do not exist (padding,
@@ -697,7 +725,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         // One online merge over the key splits, sixteen partials loaded
         // before any is used: a load feeding each step would expose one L2
         // latency per split while the MMA waits for the first unit's reader.
-        const float2* src = a.p1part + item_index(a.item_off1, it.r, it.g, 0, it.qc, nsplit1, a.NQC) * a.QC + row;
+        const float2* src = a.p1part + pass1_item_index(a, it.r, it.g, it.qc, nsplit1) * a.QC + row;
         const int64_t split_stride = (int64_t)a.NQC * a.QC;   // consecutive splits of one (g, qc)
         float mm = -INFINITY, Z = 0.f;
         for (int s0 = 0; s0 < nsplit1; s0 += 16) {
@@ -733,6 +761,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 }
 
 // ------------------------------------------------------------- host -------
+
+static_assert(sizeof(ScoreArgs) + 2 * sizeof(CUtensorMap) <= 4096, "scoring kernel parameters within 4 KB");
 
 template <class K>
 cudaError_t launch_pass(K kernel, int pass, int items, const ScoreArgs& a, cudaStream_t s, bool pdl) {

@@ -55,12 +55,25 @@ __device__ __forceinline__ int owner_of(const int32_t* off, int R, int x) {
   return lo;
 }
 
+// cu_seqlens and block offsets of a tail or gather launch: those carried in its
+// parameters (the argument must be the kernel's __grid_constant__ parameter),
+// else the device cu_seqlens and the workspace offsets describe_kernel wrote.
+__device__ __forceinline__ DescView tail_view(const TailArgs& a) {
+  if (a.desc.R > 0) return DescView{a.desc.cu, nullptr, nullptr, a.desc.blk};
+  return DescView{a.s.cu, nullptr, nullptr, a.s.blk_off};
+}
+
+__device__ __forceinline__ DescView gather_view(const GatherListArgs& g) {
+  if (g.desc.R > 0) return DescView{g.desc.cu, nullptr, nullptr, g.desc.blk};
+  return DescView{g.c.cu, nullptr, nullptr, g.blk_off};
+}
+
 // The last request is done: offsets of the compacted batch, the total, the
 // keep-bit words shared by neighbouring requests (cleared, then the edge bits
 // of every request OR-ed in), and zero counts for empty requests.  Run by
 // the whole CTA.  With no blocks at all (an empty batch, or a descriptor the
 // describe kernel rejected), every count is 0 and every keep bit is cleared.
-__device__ void finish_batch(const TailArgs& a, bool no_blocks) {
+__device__ void finish_batch(const TailArgs& a, const DescView& dv, bool no_blocks) {
   __shared__ int s_carry;
   __shared__ int s_warp[kTailWarps];
   const SelectArgs& s = a.s;
@@ -71,10 +84,10 @@ __device__ void finish_batch(const TailArgs& a, bool no_blocks) {
     for (int r = tid; r < s.R; r += blockDim.x) s.kept_count[r] = 0;
   } else {
     for (int r = tid; r < s.R; r += blockDim.x)
-      if (s.cu[r + 1] == s.cu[r]) s.kept_count[r] = 0;
+      if (dv.cu[r + 1] == dv.cu[r]) s.kept_count[r] = 0;
     // words a request covers only in part: clear, then OR in every request's part
     for (int r = tid; r < s.R; r += blockDim.x) {
-      const int tok0 = s.cu[r], L = s.cu[r + 1] - tok0;
+      const int tok0 = dv.cu[r], L = dv.cu[r + 1] - tok0;
       if (L <= 0) continue;
       const int w0 = tok0 >> 5, w1 = (tok0 + L - 1) >> 5;
       if (w0 * 32 < tok0 || w0 * 32 + 32 > tok0 + L) s.keep_bits[w0] = 0u;
@@ -82,7 +95,7 @@ __device__ void finish_batch(const TailArgs& a, bool no_blocks) {
     }
     __syncthreads();
     for (int r = tid; r < s.R; r += blockDim.x) {
-      const int tok0 = s.cu[r], L = s.cu[r + 1] - tok0;
+      const int tok0 = dv.cu[r], L = dv.cu[r + 1] - tok0;
       if (L <= 0) continue;
       const int w0 = tok0 >> 5, w1 = (tok0 + L - 1) >> 5;
       if (w0 * 32 < tok0 || w0 * 32 + 32 > tok0 + L) atomicOr(&s.keep_bits[w0], __ldcg(a.edge_bits + 2 * r));
@@ -120,12 +133,12 @@ __device__ void finish_batch(const TailArgs& a, bool no_blocks) {
 // Selection of request r by the whole CTA, then its keep bits (whole words
 // inside the request by plain stores, the first and last word's bits to the
 // edge scratch), its count and its kept-token list.
-__device__ void select_and_emit(const TailArgs& a, int r, const SelectScratch& sc) {
+__device__ void select_and_emit(const TailArgs& a, const DescView& dv, int r, const SelectScratch& sc) {
   __shared__ int s_warp[kTailWarps], s_warpb[kTailWarps];
   const SelectArgs& s = a.s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b0 = s.blk_off[r], nb = s.blk_off[r + 1] - b0;
-  const int tok0 = s.cu[r], L = s.cu[r + 1] - tok0;
+  const int b0 = dv.blk[r], nb = dv.blk[r + 1] - b0;
+  const int tok0 = dv.cu[r], L = dv.cu[r + 1] - tok0;
   const int kept = select_request(s.block_scores + b0, nb, L, s.G, s.top_p, s.sink_keep, s.tail_keep, sc, s.status);
   const int w0 = tok0 >> 5, w1 = (tok0 + L - 1) >> 5;
   for (int w = w0 + tid; w <= w1; w += blockDim.x) {
@@ -182,7 +195,7 @@ __device__ void select_and_emit(const TailArgs& a, int r, const SelectScratch& s
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailArgs a) {
+__global__ void __launch_bounds__(kTailThreads) tail_kernel(const __grid_constant__ TailArgs a) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ unsigned char s_dyn[];
@@ -192,9 +205,10 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailArgs a) {
   __shared__ int s_nsel, s_last;
   const SelectArgs& s = a.s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nb_total = s.blk_off[s.R];   // 0 if the describe kernel rejected the descriptor
+  const DescView dv = tail_view(a);
+  const int nb_total = dv.blk[s.R];   // 0 if the describe kernel rejected the descriptor
   if (nb_total == 0) {
-    if (blockIdx.x == 0) finish_batch(a, true);
+    if (blockIdx.x == 0) finish_batch(a, dv, true);
     return;
   }
   const int b0 = blockIdx.x * a.bpc;
@@ -205,9 +219,9 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailArgs a) {
   // tokens of the packed batch) and each block's 1/(H_q n_eff).
   if (tid <= nown) {
     const int b = b0 + min(tid, nown - 1);
-    const int r = owner_of(s.blk_off, s.R, b);
-    const int i = b - s.blk_off[r];
-    const int tok0 = s.cu[r], L = s.cu[r + 1] - tok0;
+    const int r = owner_of(dv.blk, s.R, b);
+    const int i = b - dv.blk[r];
+    const int tok0 = dv.cu[r], L = dv.cu[r + 1] - tok0;
     if (tid < nown) {
       s_bstart[tid] = tok0 + i * s.G;
       s_inv[tid] = 1.0f / float(s.Hq * min(s.n, L));
@@ -256,10 +270,10 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailArgs a) {
   // completes.  The acquire-release increments publish this CTA's block means
   // and, for the CTA that completes a request, make every other CTA's visible.
   if (tid == 0) {
-    const int r_first = owner_of(s.blk_off, s.R, b0), r_last = owner_of(s.blk_off, s.R, b1 - 1);
+    const int r_first = owner_of(dv.blk, s.R, b0), r_last = owner_of(dv.blk, s.R, b1 - 1);
     int nsel = 0;
     for (int r = r_first; r <= r_last; ++r) {
-      const int f = s.blk_off[r], e = s.blk_off[r + 1];
+      const int f = dv.blk[r], e = dv.blk[r + 1];
       if (e == f) continue;   // empty request (no blocks)
       const int ctas = (e - 1) / a.bpc - f / a.bpc + 1;
       if (ctas == 1 || add_acq_rel(a.counters + r, 1) == ctas - 1) s_sel[nsel++] = r;
@@ -270,13 +284,13 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailArgs a) {
   const int nsel = s_nsel;
   if (nsel == 0) return;
   const SelectScratch sc = carve_select(s_dyn, a.nbp);
-  for (int k = 0; k < nsel; ++k) select_and_emit(a, s_sel[k], sc);
+  for (int k = 0; k < nsel; ++k) select_and_emit(a, dv, s_sel[k], sc);
   if (tid == 0) {
     // With one request (or this CTA completing all of them) nothing else is pending.
     if (nsel == a.nonempty || add_acq_rel(a.counters + s.R, nsel) + nsel == a.nonempty) s_last = 1;
   }
   __syncthreads();
-  if (s_last) finish_batch(a, false);
+  if (s_last) finish_batch(a, dv, false);
 }
 
 // The gather of the fused path: output row o belongs to the request r with
@@ -285,10 +299,11 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const TailArgs a) {
 // same loads), and its input row follows from the block's first token.  One
 // warp per output row, 16-byte vectors, eight in flight per lane; block 0
 // appends the drop-history record.
-__global__ void __launch_bounds__(256) gather_list_kernel(const GatherListArgs g) {
+__global__ void __launch_bounds__(256) gather_list_kernel(const __grid_constant__ GatherListArgs g) {
   pdl_trigger();
   pdl_wait();
   const CompactArgs& a = g.c;
+  const DescView dv = gather_view(g);
   const int total = min(*a.total_kept, a.T);
   if (blockIdx.x == 0 && threadIdx.x == 0 && a.history) {
     bool full = false;
@@ -312,7 +327,7 @@ __global__ void __launch_bounds__(256) gather_list_kernel(const GatherListArgs g
   for (int o = warp; o < total; o += nwarps) {
     const int r = owner_of(a.cu_out, a.R, o);
     const int j = o - a.cu_out[r];
-    const int base = g.blk_off[r];
+    const int base = dv.blk[r];
     // 32-way search: each lane probes one of 32 evenly spaced kept blocks and
     // the last probe at or below j narrows the range (one round for up to 32
     // kept blocks, two for up to 1024).
@@ -329,8 +344,8 @@ __global__ void __launch_bounds__(256) gather_list_kernel(const GatherListArgs g
       n = min(step, n - last * step);
     }
     if (n != 1) continue;
-    const int t = a.cu[r] + g.kept_blk[base + lo] * g.G + (j - g.kept_off[base + lo]);
-    if (t < a.cu[r] || t >= a.cu[r + 1] || t >= a.T) continue;   // never for a consistent batch
+    const int t = dv.cu[r] + g.kept_blk[base + lo] * g.G + (j - g.kept_off[base + lo]);
+    if (t < dv.cu[r] || t >= dv.cu[r + 1] || t >= a.T) continue;   // never for a consistent batch
     if (lane == 0 && a.kept_index) a.kept_index[o] = t;
     if (a.hidden_in) {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(a.hidden_in) + (int64_t)t * a.row_bytes);
@@ -351,6 +366,8 @@ __global__ void __launch_bounds__(256) gather_list_kernel(const GatherListArgs g
 }
 
 }  // namespace
+
+static_assert(sizeof(TailArgs) <= 4096 && sizeof(GatherListArgs) <= 4096, "tail kernel parameters within 4 KB");
 
 int tail_blocks_per_cta(int G) {
   int bpc = G > 0 ? kTailThreads / G : 1;   // about one token per thread in the finalize phase

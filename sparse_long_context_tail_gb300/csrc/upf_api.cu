@@ -528,6 +528,26 @@ upf::DescribeArgs describe_args(const upf_ctx* ctx, const upf_batch* b, const Pl
   return a;
 }
 
+// The tables describe_kernel would build, from cu_seqlens_host (the batch has
+// at most kInlineReqs requests).
+void fill_desc(const upf_batch* b, const Plan& pl, upf::DescInline* d) {
+  const int32_t* cu = b->cu_seqlens_host;
+  const int units = pl.Hkv * pl.NQC;
+  int o1 = 0, o2 = 0, ob = 0;
+  d->R = pl.R;
+  for (int r = 0; r <= pl.R; ++r) {
+    d->cu[r] = cu[r];
+    d->off1[r] = o1;
+    d->off2[r] = o2;
+    d->blk[r] = ob;
+    if (r == pl.R) break;
+    const int L = cu[r + 1] - cu[r];
+    o1 += units * ceil_div(L, pl.KS1);
+    o2 += units * ceil_div(L, pl.KS2);
+    ob += ceil_div(L, pl.G);
+  }
+}
+
 // Arguments of the fused tail; with_lists: the kept-block lists for the
 // gather; cu_out / total_kept nullable.
 upf::TailArgs tail_args(const upf::SelectArgs& se, const Plan& pl, void* ws, bool with_lists, int32_t* cu_out,
@@ -544,6 +564,7 @@ upf::TailArgs tail_args(const upf::SelectArgs& se, const Plan& pl, void* ws, boo
   t.nonempty = pl.nonempty;
   t.bpc = upf::tail_blocks_per_cta(pl.G);
   t.nbp = ((pl.max_nb > 0 ? pl.max_nb : 1) + 7) & ~7;
+  t.desc.R = 0;
   return t;
 }
 
@@ -938,9 +959,19 @@ upf_status upf_select_tokens(upf_ctx* ctx, const upf_batch* batch, const upf_par
   if ((st = check_compact_io(pl, keep_bits, io, ctx->device)) != UPF_OK) return st;
   DeviceGuard guard(ctx->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const upf::DescribeArgs da = describe_args(ctx, batch, pl, ws);
-  UPF_LAUNCH(staged(ctx, kDescribe, s, [&] { return upf::launch_describe(da, s, false); }), "describe");
   upf::ScoreArgs sa = score_args(ctx, batch, pl, q, q_row_stride, k, k_row_stride, ws);
+  // Batches of up to kInlineReqs requests on the tensor-core path carry the
+  // descriptor tables in the kernel parameters: no describe launch, and pass 1
+  // checks the device cu_seqlens and clears the tail's counters instead.
+  const bool carried = pl.use_tc && fused_tail(pl) && pl.R <= upf::kInlineReqs && pl.items1 > 0 && pl.items2 > 0;
+  if (carried) {
+    fill_desc(batch, pl, &sa.desc);
+    sa.counters = at<int32_t>(ws, pl.off_ctr);
+    sa.ncounters = pl.R + 1;
+  } else {
+    const upf::DescribeArgs da = describe_args(ctx, batch, pl, ws);
+    UPF_LAUNCH(staged(ctx, kDescribe, s, [&] { return upf::launch_describe(da, s, false); }), "describe");
+  }
   UPF_LAUNCH(staged(ctx, kPass1, s, [&] { return upf::launch_score_pass1(sa, s, true); }), "score pass 1");
   UPF_LAUNCH(staged(ctx, kPass2, s, [&] { return upf::launch_score_pass2(sa, s, true); }), "score pass 2");
   upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC * pl.pw, sa.part, nullptr, scores, block_scores,
@@ -948,7 +979,8 @@ upf_status upf_select_tokens(upf_ctx* ctx, const upf_batch* batch, const upf_par
   if (fused_tail(pl)) {
     // finalize + block means + select + kept-block lists + compacted offsets
     // in one launch, then the gather driven by the kept-block lists
-    const upf::TailArgs ta = tail_args(se, pl, ws, true, io->cu_seqlens_out, io->total_kept);
+    upf::TailArgs ta = tail_args(se, pl, ws, true, io->cu_seqlens_out, io->total_kept);
+    if (carried) ta.desc = sa.desc;
     UPF_LAUNCH(staged(ctx, kSelect, s, [&] { return upf::launch_tail(ta, s, true); }), "finalize and select");
     upf::GatherListArgs ga;
     ga.c = compact_args(ctx, batch, pl, keep_bits, io, ws);
@@ -958,6 +990,8 @@ upf_status upf_select_tokens(upf_ctx* ctx, const upf_batch* batch, const upf_par
     ga.kept_off = ta.kept_off;
     ga.kept_nblk = ta.kept_nblk;
     ga.G = pl.G;
+    ga.desc.R = 0;
+    if (carried) ga.desc = sa.desc;
     UPF_LAUNCH(staged(ctx, kCompactGather, s, [&] { return upf::launch_gather_list(ga, s, true); }), "compact gather");
     return UPF_OK;
   }

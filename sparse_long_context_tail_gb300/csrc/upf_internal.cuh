@@ -35,6 +35,29 @@ constexpr int kTcPartials = 1;
 // in SM clock cycles (about 2 s at 2 GHz).
 constexpr long long kDefaultWaitCycles = 4000000000LL;
 
+// Descriptor tables of a batch (cu_seqlens, the first item of each request in
+// pass 1 and pass 2, the first block of each request), computed on the host
+// from cu_seqlens_host.  The fused path carries them in the kernel parameters
+// for batches of up to kInlineReqs requests, so no kernel has to build them on
+// the device first; larger batches (and the separate entry points) keep them
+// in the workspace, written by describe_kernel.
+constexpr int kInlineReqs = 64;
+struct DescInline {
+  int32_t R;                     // 0: not carried (read the workspace tables)
+  int32_t cu[kInlineReqs + 1];
+  int32_t off1[kInlineReqs + 1];
+  int32_t off2[kInlineReqs + 1];
+  int32_t blk[kInlineReqs + 1];
+};
+
+// The tables one kernel reads, wherever they live.
+struct DescView {
+  const int32_t* cu;
+  const int32_t* off1;
+  const int32_t* off2;
+  const int32_t* blk;
+};
+
 struct ScoreArgs {
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
@@ -56,7 +79,10 @@ struct ScoreArgs {
   int32_t pw;                // partial rows per item row / per (g, qc): kTcPartials or 1
   int32_t* status;
   long long wait_limit;      // pipeline waits of the tensor-core kernels (cycles)
+  int32_t* counters;         // [ncounters] cleared by pass 1 for the tail kernel when
+  int32_t ncounters;         //   desc.R > 0 (describe_kernel clears them otherwise)
   int32_t qhead[kMaxHeads];  // q heads of group g at [g*gamma, (g+1)*gamma)
+  DescInline desc;           // desc.R > 0: these tables, and the device cu_seqlens only checked
 };
 
 struct DescribeArgs {
@@ -106,6 +132,7 @@ struct TailArgs {
   int32_t nonempty;     // requests with at least one token (host value)
   int32_t bpc;          // blocks per CTA
   int32_t nbp;          // selection scratch capacity in blocks (multiple of 8, >= max_nb)
+  DescInline desc;      // desc.R > 0: cu and block offsets from here, not s.cu / s.blk_off
 };
 
 struct CompactArgs {
@@ -208,6 +235,7 @@ struct GatherListArgs {
   const int32_t* kept_off;
   const int32_t* kept_nblk;
   int32_t G;
+  DescInline desc;          // desc.R > 0: cu and block offsets from here, not c.cu / blk_off
 };
 cudaError_t launch_gather_list(const GatherListArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_revive(const ReviveArgs& a, cudaStream_t s, bool pdl = false);

@@ -417,6 +417,39 @@ def test_inconsistent_device_cu_seqlens_is_reported(sel):
     assert sel.status() == 1
 
 
+@pytest.mark.parametrize("R", [64, 70])
+def test_batches_at_and_past_the_carried_descriptor_limit(sel, R):
+    """Up to 64 requests the fused call carries the batch's descriptor tables in
+    the kernel parameters; past that the describe kernel builds them on the
+    device.  Both routes against the oracle, with requests shorter than n."""
+    rng = np.random.default_rng(20 + R)
+    lengths = [int(x) for x in rng.integers(1, 400, size=R)]
+    spec = wl.WorkloadSpec(f"many-{R}", lengths, 8, 2, 64, 64, n_tail=32, block=16, seed=R)
+    w = wl.generate(spec)
+    p = params_of(spec)
+    out, status, inputs = run_gpu(sel, w, p)
+    check(w, p, out, status, inputs)
+
+
+@pytest.mark.parametrize("R", [2, 70])
+def test_inconsistent_device_cu_seqlens_in_the_fused_call(sel, R):
+    """A device cu_seqlens whose total disagrees with the host copy is reported
+    by both descriptor routes (carried tables and device-built ones)."""
+    spec = wl.WorkloadSpec("cu-mismatch", [300] * R, 8, 2, 64, 64, n_tail=32, block=16, seed=9)
+    w = wl.generate(spec)
+    q = _up(w.q_full_bits().view(np.int16)).view(torch.bfloat16)
+    k = _up(w.k_bits.view(np.int16)).view(torch.bfloat16)
+    bad = w.cu_seqlens.copy()
+    bad[-1] -= 7
+    sel.select_tokens(q, k, w.cu_seqlens, _up(bad), spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                      params=params_of(spec))
+    torch.cuda.synchronize()
+    assert sel.status() == 1
+    # the context stays usable
+    out, status, inputs = run_gpu(sel, w, params_of(spec), hidden=False)
+    assert status == 0
+
+
 def test_repeat_calls_are_deterministic(sel):
     spec = small_spec("det", SMALL[1][1])
     w = wl.generate(spec)
