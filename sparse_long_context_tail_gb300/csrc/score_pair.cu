@@ -187,6 +187,7 @@ __device__ uint32_t pair_setup(const ScoreArgs& a, const PSmem& sm, const PGeo& 
 
 // Producer (one lane): this CTA's half of the query chunk, then its 128 keys
 // of every pair tile, stage by stage.  Returns the stage loads issued.
+template <bool kDescending>
 __device__ int pair_produce(const ScoreArgs& a, const CUtensorMap* tq_map, const CUtensorMap* tk_map, const PSmem& sm,
                             const PGeo& geo, const ItemTC& it, int rows_c, int U, int k0, int ntiles, uint32_t rank) {
   const int BQ = a.q_box_rows;
@@ -208,7 +209,7 @@ __device__ int pair_produce(const ScoreArgs& a, const CUtensorMap* tq_map, const
   const int total = ntiles * geo.spt;
   int q = 0, st = 0, part = 0;
   uint32_t ph = 0;
-  int key = it.tok0 + k0 + int(rank) * kHalf;
+  int key = it.tok0 + k0 + int(rank) * kHalf + (kDescending ? (ntiles - 1) * kPairTile : 0);
   for (int n = 0; n < total; ++n, ++q) {
     if (paborted(sm)) return q;
     if (!mbar_wait_idle(b_empty(sm, st), ph ^ 1u, a.wait_limit, kIdleNs)) {
@@ -220,7 +221,7 @@ __device__ int pair_produce(const ScoreArgs& a, const CUtensorMap* tq_map, const
     for (int ss = 0; ss < geo.sps; ++ss)
       tma_load_3d(dst + uint32_t(ss * geo.slice_bytes), tk_map, (part * geo.sps + ss) * 64, it.g, key, b_full(sm, st));
     if (++st == geo.NS) { st = 0; ph ^= 1u; }
-    if (++part == geo.spt) { part = 0; key += kPairTile; }
+    if (++part == geo.spt) { part = 0; key += kDescending ? -kPairTile : kPairTile; }
   }
   return q;
 }
@@ -485,7 +486,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   const uint32_t tmem = pair_setup(a, sm, geo, rows_c, rank);
   int issued = 0;
   if (warp == kProducerWarp) {
-    if (lane == 0) issued = pair_produce(a, &tq_map, &tk_map, sm, geo, it, rows_c, U, k0, ntiles, rank);
+    if (lane == 0) issued = pair_produce<false>(a, &tq_map, &tk_map, sm, geo, it, rows_c, U, k0, ntiles, rank);
     if (blockIdx.x == 0) desc_check(a, lane);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
@@ -519,8 +520,11 @@ __device__ void pair_pass2_epilogue(const ScoreArgs& a, const PSmem& sm, const I
   const uint32_t nlse_s = smem_u32(sm.nlse);
   bool ok = true;
   int uidx = 0;
+  // Tiles run from the item's last keys to its first: pass 1 read the keys in
+  // ascending order, so the last ones it read may still be in L2.
+  const int klast = k0 + (ntiles - 1) * kPairTile + int(rank) * kHalf;   // this CTA's first key of the last tile
   for (int i = 0; i < ntiles; ++i) {
-    const int kt = k0 + i * kPairTile + int(rank) * kHalf;   // this CTA's first key of the tile
+    const int kt = klast - i * kPairTile;   // this CTA's first key of the tile
     const int key = kt + krow;
     const bool masked = kt + kHalf - 1 > it.L - a.n;
     uint64_t acc0 = pack2(0.f, 0.f), acc1 = pack2(0.f, 0.f);
@@ -531,7 +535,7 @@ __device__ void pair_pass2_epilogue(const ScoreArgs& a, const PSmem& sm, const I
         break;
       }
       if (u == 0 && cb == 0 && i >= lag) {   // tile i - lag is complete: write it out
-        const int kprev = key - lag * kPairTile;
+        const int kprev = key + lag * kPairTile;
         if (kprev < k1) out[kprev] = [&] {
             const float* r = sm.red + ((i - lag) % kRedTiles) * kW * 128 + krow;
             float t = r[0];
@@ -564,7 +568,7 @@ __device__ void pair_pass2_epilogue(const ScoreArgs& a, const PSmem& sm, const I
   pepi_bar();
   if (ok && cb == 0 && !paborted(sm))
     for (int i = max(0, ntiles - lag); i < ntiles; ++i) {
-      const int key = k0 + i * kPairTile + int(rank) * kHalf + krow;
+      const int key = klast - i * kPairTile + krow;
       if (key < k1) {
         const float* r = sm.red + (i % kRedTiles) * kW * 128 + krow;
         float t = r[0];
@@ -596,7 +600,7 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
   const uint32_t tmem = pair_setup(a, sm, geo, rows_c, rank);
   int issued = 0;
   if (warp == kProducerWarp) {
-    if (lane == 0) issued = pair_produce(a, &tq_map, &tk_map, sm, geo, it, rows_c, U, k0, ntiles, rank);
+    if (lane == 0) issued = pair_produce<true>(a, &tq_map, &tk_map, sm, geo, it, rows_c, U, k0, ntiles, rank);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       if (rank == 0) pair_mma<true>(a, sm, geo, ntiles, U, tmem, true);

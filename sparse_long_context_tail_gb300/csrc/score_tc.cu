@@ -232,7 +232,7 @@ __device__ __forceinline__ bool wait_slot_fast(const ScoreArgs& a, const Smem& s
 // while one elected lane issues the copies.
 __device__ int produce(const ScoreArgs& a, const CUtensorMap* tq_map, const CUtensorMap* tk_map, const Smem& sm,
                        const Geo& geo, const ItemTC& it, int rows_c, int k0, int ntiles, bool may_repeat,
-                       bool warp_wide) {
+                       bool warp_wide, bool descending = false) {
   const bool leader = warp_wide ? elect_one() : true;
   const int BQ = a.q_box_rows;
   const int boxes = rows_c / BQ;
@@ -257,7 +257,8 @@ __device__ int produce(const ScoreArgs& a, const CUtensorMap* tq_map, const CUte
       }
       if (*reinterpret_cast<volatile int*>(sm.redo) == 0) break;
     }
-    int part = 0, key = it.tok0 + k0;
+    const int step = descending ? -geo.tile_keys : geo.tile_keys;
+    int part = 0, key = it.tok0 + k0 + (descending ? (ntiles - 1) * geo.tile_keys : 0);
     for (int n = 0; n < total; ++n, ++q) {
       if (!mbar_wait_idle(bar_empty(sm, st), ph ^ 1u, a.wait_limit, kIdleNs)) {
         abort_with_timeout(a, sm);
@@ -271,7 +272,7 @@ __device__ int produce(const ScoreArgs& a, const CUtensorMap* tq_map, const CUte
                       bar_full(sm, st));
       }
       if (++st == geo.NS) { st = 0; ph ^= 1u; }
-      if (++part == geo.spt) { part = 0; key += geo.tile_keys; }
+      if (++part == geo.spt) { part = 0; key += step; }
     }
   }
   return q;
@@ -638,8 +639,10 @@ __device__ __forceinline__ void pass2_epilogue(const ScoreArgs& a, const Smem& s
   static_assert(kRedTiles >= 6, "rows are read lag tiles after their stores and rewritten lag tiles later");
   bool ok = true;
   int uidx = 0;
+  // Tiles run from the item's last keys to its first: pass 1 read the keys in
+  // ascending order, so the last ones it read may still be in L2.
   for (int i = 0; i < ntiles; ++i) {
-    const int kt = k0 + i * geo.tile_keys;
+    const int kt = k0 + (ntiles - 1 - i) * geo.tile_keys;
     const int key = kt + krow;
     const bool masked = kt + geo.tile_keys - 1 > it.L - a.n;
     uint64_t acc0 = pack2(0.f, 0.f), acc1 = pack2(0.f, 0.f);
@@ -650,7 +653,7 @@ __device__ __forceinline__ void pass2_epilogue(const ScoreArgs& a, const Smem& s
         break;
       }
       if (u == 0 && cb == 0 && i >= lag) {   // tile i - lag is complete: write it out
-        const int kprev = key - lag * geo.tile_keys;
+        const int kprev = key + lag * geo.tile_keys;
         if (kprev < k1) out[kprev] = red_sum(sm.red, i - lag, krow);
       }
       const int col0 = u * geo.unit_cols + cb * 32;
@@ -679,7 +682,7 @@ __device__ __forceinline__ void pass2_epilogue(const ScoreArgs& a, const Smem& s
   epi_bar();
   if (ok && cb == 0 && !aborted(sm))
     for (int i = max(0, ntiles - lag); i < ntiles; ++i) {
-      const int key = k0 + i * geo.tile_keys + krow;
+      const int key = k0 + (ntiles - 1 - i) * geo.tile_keys + krow;
       if (key < k1) out[key] = red_sum(sm.red, i, krow);
     }
 }
@@ -705,7 +708,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 
   int issued = 0;
   if (warp == kProducerWarp) {
-    if (lane == 0) issued = produce(a, &tq_map, &tk_map, sm, geo, it, rows_c, k0, ntiles, false, false);
+    if (lane == 0) issued = produce(a, &tq_map, &tk_map, sm, geo, it, rows_c, k0, ntiles, false, false, true);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       if (U >= 2) issue_mma<true>(a, sm, geo, ntiles, U, tmem, true, false, false);

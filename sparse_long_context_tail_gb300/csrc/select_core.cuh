@@ -277,18 +277,20 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
     }
   }
   __syncthreads();
-  // Exempt blocks: overlap with [0, sink) or [L - tail, L).
+  // Exempt blocks (overlap with [0, sink) or [L - tail, L)) and the kept
+  // tokens, each block by the thread that owns it in this loop.
   const int sink_hi = min(sink_keep, L);
   const int tail_lo = max(0, L - tail_keep);
+  int cnt = 0;
   for (int i = tid; i < nb; i += blockDim.x) {
     const int lo = i * G, hi = min(L, lo + G);
-    if (lo < sink_hi || hi > tail_lo) sc.keep[i] = 1;
+    bool kept = sc.keep[i] != 0;
+    if (lo < sink_hi || hi > tail_lo) {
+      sc.keep[i] = 1;
+      kept = true;
+    }
+    if (kept) cnt += hi - lo;
   }
-  __syncthreads();
-  // Kept tokens.
-  int cnt = 0;
-  for (int i = tid; i < nb; i += blockDim.x)
-    if (sc.keep[i]) cnt += min(L, (i + 1) * G) - i * G;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
   if (lane == 0 && cnt) atomicAdd(&s_cnt, cnt);

@@ -25,6 +25,8 @@
 // finalize kernel (partials in index order, then tokens lane-strided within a
 // warp and a fixed shuffle tree), so the fused and the separate entry points
 // give the same bits.
+#include <climits>
+
 #include "select_core.cuh"
 #include "upf_internal.cuh"
 
@@ -330,21 +332,36 @@ __global__ void __launch_bounds__(256) gather_list_kernel(const __grid_constant_
     const int base = dv.blk[r];
     // 32-way search: each lane probes one of 32 evenly spaced kept blocks and
     // the last probe at or below j narrows the range (one round for up to 32
-    // kept blocks, two for up to 1024).
+    // kept blocks, two for up to 1024).  Each probe also loads its block's
+    // index, so when the probes are single blocks the answer is already in a
+    // lane's registers: one dependent round trip less before the row's copy.
     int lo = 0, n = g.kept_nblk[r];
     if (n <= 0) continue;   // never for a consistent batch
+    int kb = -1, koff = 0;
     while (n > 1) {
       const int step = (n + 31) >> 5;
       const int at = lane * step;
-      const bool le = at < n && g.kept_off[base + lo + at] <= j;
-      const unsigned below = __ballot_sync(0xffffffffu, le);   // lane 0 always: offset 0 <= j
+      int off = INT_MAX, blk = 0;
+      if (at < n) {
+        off = g.kept_off[base + lo + at];
+        blk = g.kept_blk[base + lo + at];
+      }
+      const unsigned below = __ballot_sync(0xffffffffu, off <= j);   // lane 0 always: offset 0 <= j
       if (!below) break;   // never for a consistent batch
       const int last = 31 - __clz(below);
       lo += last * step;
       n = min(step, n - last * step);
+      if (step == 1) {   // the probes were the blocks themselves
+        kb = __shfl_sync(0xffffffffu, blk, last);
+        koff = __shfl_sync(0xffffffffu, off, last);
+      }
     }
     if (n != 1) continue;
-    const int t = dv.cu[r] + g.kept_blk[base + lo] * g.G + (j - g.kept_off[base + lo]);
+    if (kb < 0) {   // one kept block, or the search ended on a range of blocks
+      kb = g.kept_blk[base + lo];
+      koff = g.kept_off[base + lo];
+    }
+    const int t = dv.cu[r] + kb * g.G + (j - koff);
     if (t < dv.cu[r] || t >= dv.cu[r + 1] || t >= a.T) continue;   // never for a consistent batch
     if (lane == 0 && a.kept_index) a.kept_index[o] = t;
     if (a.hidden_in) {
