@@ -322,6 +322,23 @@ upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p
       }
     const char* path = std::getenv("UPF_SCORE_PATH");
     pl->use_tc = pl->q_box_rows > 0 && !(path && std::strcmp(path, "simt") == 0);
+    // Small batches: when even one key tile per item would leave SMs without
+    // an item, smaller query chunks spread the same work over more SMs (every
+    // chunk reads its keys again, from L2) and each item runs fewer units in a
+    // row.  Halved down to one 128-row tile while the items stay below one
+    // per SM.
+    if (pl->use_tc) {
+      const int tile = upf::score_tc_key_tile(1, pl->d);
+      auto most_items = [&](int qc) {
+        long long items = 0;
+        for (int r = 0; r < pl->R; ++r)
+          items += (long long)pl->Hkv * ceil_div(pl->QR, qc) *
+                   ceil_div(b->cu_seqlens_host[r + 1] - b->cu_seqlens_host[r], tile);
+        return items;
+      };
+      while (pl->QC > 128 && most_items(pl->QC) < upf::kPlanSMs) pl->QC = ((pl->QC / 2 + 127) / 128) * 128;
+      pl->NQC = ceil_div(pl->QR, pl->QC);
+    }
     // Key splits: the tensor-core kernels hold one CTA per SM, so one wave of
     // about one item per SM; the CUDA-core kernels want a few waves.  The split
     // depends only on the batch and parameters (never on the device), so

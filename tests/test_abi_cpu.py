@@ -136,6 +136,10 @@ def test_scoring_work_split_is_near_the_best_whole_tile_split(lib):
         gamma = s.num_q_heads // s.num_kv_heads
         qr = gamma * s.n_tail
         qc = min(-(-qr // 128) * 128, 512 if s.head_dim <= 128 else (128 if qr <= 256 else 256))
+        tile1 = 256 if s.head_dim <= 128 else 128      # pass-1 key tile of the single-CTA kernels
+        # small batches: halve the chunk while even one tile per item leaves SMs idle
+        while qc > 128 and s.num_kv_heads * -(-qr // qc) * sum(-(-L // tile1) for L in s.lengths) < 152:
+            qc = -(-(qc // 2) // 128) * 128
         nqc = -(-qr // qc)
         units = s.num_kv_heads * nqc
         for ks, n, tile in ((ks1, n1, 256 if ctas == 2 or s.head_dim <= 128 else 128),

@@ -500,7 +500,10 @@ def _select_only(sel, scores_np, cu, block, top_p, sink=128, tail=128):
 def test_select_ties_take_lower_blocks_first(sel):
     """Equal block scores at the boundary enter in block-index order (the oracle's tie rule)."""
     rng = np.random.default_rng(3)
-    for G, L, top_p in [(64, 64 * 300, 0.5), (32, 32 * 1000 + 17, 0.37), (16, 16 * 5000, 0.9)]:
+    # large and small requests, partial last blocks
+    for G, L, top_p in [(64, 64 * 300, 0.5), (32, 32 * 1000 + 17, 0.37), (16, 16 * 5000, 0.9),
+                        (64, 64 * 200, 0.5), (32, 32 * 37 + 5, 0.9), (16, 16 * 256, 0.3), (8, 8 * 257, 0.6),
+                        (64, 64 * 3 + 1, 0.99)]:
         nb = -(-L // G)
         levels = np.array([0.0, 1.0, 2.0, 4.0], dtype=np.float32)    # few distinct values: many ties
         b = levels[rng.integers(0, 4, size=nb)]
