@@ -30,6 +30,7 @@ namespace upf {
 
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kCountSel = 256;   // requests of up to this many blocks are ranked by counting
 
 // Shared memory the select core needs beyond its static arrays, for a request
 // of up to nbp blocks (nbp a multiple of 8).
@@ -176,7 +177,20 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
     const unsigned long long total = sel_block_sum(part, s_u64);
     // Mass the selected prefix must reach: the smallest integer >= top_p * total.
     const unsigned long long target = (unsigned long long)ceil((double)top_p * (double)total);
-    if (target > 0) {
+    if (target > 0 && nb <= kCountSel) {
+      // Small request: block i's thread adds the masses of every block ranked
+      // before it (score desc, index asc) and keeps i while that sum is below
+      // the target: the radix select's set, without its rounds and barriers.
+      if (tid < nb) {
+        const unsigned long long ki = ((unsigned long long)sc.bits[tid] << 32) | (0xFFFFFFFFu - uint32_t(tid));
+        unsigned long long before = 0;
+        for (int j = 0; j < nb; ++j) {
+          const unsigned long long kj = ((unsigned long long)sc.bits[j] << 32) | (0xFFFFFFFFu - uint32_t(j));
+          if (kj > ki) before += sc.m[j];
+        }
+        if (before < target) sc.keep[tid] = 1;
+      }
+    } else if (target > 0) {
       uint32_t prefix = 0, pmask = 0;
       unsigned long long above = 0;   // mass of blocks ranked strictly before the candidates
       const int nb_pad = (nb + 31) & ~31;   // whole warps take part in the aggregation
