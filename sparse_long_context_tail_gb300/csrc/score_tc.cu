@@ -579,8 +579,11 @@ __device__ __forceinline__ void pass1_epilogue(const ScoreArgs& a, const Smem& s
 __global__ void __launch_bounds__(kThreadsTC, 1)
     score_pass1_tc(const __grid_constant__ CUtensorMap tq_map, const __grid_constant__ CUtensorMap tk_map,
                    const __grid_constant__ ScoreArgs a) {
-  pdl_trigger();
+  // Wait, then let pass 2 launch: pass 2 may read the queries and keys before
+  // its own wait, so it must not start before this kernel's predecessor (which
+  // may have written them) is complete.
   pdl_wait();
+  pdl_trigger();
   extern __shared__ unsigned char smem_raw[];
   const int item = blockIdx.x;
   if (!item_exists(a, item, false)) return;
@@ -690,8 +693,15 @@ __device__ __forceinline__ void pass2_epilogue(const ScoreArgs& a, const Smem& s
 __global__ void __launch_bounds__(kThreadsTC, 1)
     score_pass2_tc(const __grid_constant__ CUtensorMap tq_map, const __grid_constant__ CUtensorMap tk_map,
                    const __grid_constant__ ScoreArgs a) {
+  // With the descriptor in the parameters, nothing before the -lse merge reads
+  // what pass 1 writes: the set-up, the query and key loads and the first
+  // MMAs run while pass 1's last CTAs finish, and only the epilogue waits for
+  // pass 1 (which launched this kernel after its own predecessor completed).
+  // Tables in the workspace come from the describe kernel, so then every
+  // thread waits first.
+  const bool early = a.desc.R > 0;
   pdl_trigger();
-  pdl_wait();
+  if (!early) pdl_wait();
   extern __shared__ unsigned char smem_raw[];
   const int item = blockIdx.x;
   if (!item_exists(a, item, true)) return;
@@ -715,6 +725,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       else issue_mma<false>(a, sm, geo, ntiles, U, tmem, true, false, false);
     }
   } else {
+    if (early) pdl_wait();
     // lse2 of every query row of the chunk from the pass-1 partials (all key
     // splits), stored negated; -inf marks rows that do not exist (padding,
     // or positions before the request start).  The MMA runs meanwhile: the
@@ -725,29 +736,31 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       int t = -1;
       if (row < rows_c) {
         t = it.L - a.n + (it.qc * a.QC + row) % a.n;
-        // One online merge over the key splits, sixteen partials loaded
-        // before any is used: a load feeding each step would expose one L2
-        // latency per split while the MMA waits for the first unit's reader.
+        // One merge over the key splits, up to 24 partials loaded before any
+        // is used (a load feeding each step would expose one L2 latency per
+        // split while the MMA waits for the first unit's reader): the largest
+        // m first, then the rescaled sums.
         const float2* src = a.p1part + pass1_item_index(a, it.r, it.g, it.qc, nsplit1) * a.QC + row;
         const int64_t split_stride = (int64_t)a.NQC * a.QC;   // consecutive splits of one (g, qc)
         float mm = -INFINITY, Z = 0.f;
-        for (int s0 = 0; s0 < nsplit1; s0 += 16) {
-          float2 pp[16];
+        for (int s0 = 0; s0 < nsplit1; s0 += 24) {
+          float2 pp[24];
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
+          for (int k = 0; k < 24; ++k)
             pp[k] = s0 + k < nsplit1 ? src[(s0 + k) * split_stride] : make_float2(-INFINITY, 0.f);
+          float mb = -INFINITY;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            if (!(pp[k].y > 0.f)) continue;
-            if (pp[k].x > mm) {
-              Z = Z * exp2f(mm - pp[k].x) + pp[k].y;
-              mm = pp[k].x;
-            } else {
-              Z += pp[k].y * exp2f(pp[k].x - mm);
-            }
+          for (int k = 0; k < 24; ++k)
+            if (pp[k].y > 0.f) mb = fmaxf(mb, pp[k].x);
+          if (mb > mm) {
+            Z = mm > -INFINITY ? Z * ex2_approx(mm - mb) : 0.f;
+            mm = mb;
           }
+#pragma unroll
+          for (int k = 0; k < 24; ++k)
+            if (pp[k].y > 0.f) Z += pp[k].y * ex2_approx(pp[k].x - mm);
         }
-        if (Z > 0.f && t >= 0) l2 = mm + log2f(Z);
+        if (Z > 0.f && t >= 0) l2 = mm + lg2_approx(Z);
         else t = -1;
       }
       sm.nlse[row] = -l2;
