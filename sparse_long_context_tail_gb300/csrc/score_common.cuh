@@ -81,6 +81,46 @@ __device__ __forceinline__ int64_t pass1_item_index(const ScoreArgs& a, int r, i
   return item_index(a.item_off1, r, g, 0, qc, nsplit1, a.NQC);
 }
 
+// Pass 2's entry for chunk row `row` of item it: -lse2 of the row's query,
+// merged from the pass-1 partials (m2, Z) of all nsplit1 key splits, and the
+// query's position; -inf and -1 for rows that do not exist (padding, or
+// positions before the request start).  Up to 24 partials are loaded before
+// any is used (a load feeding each step would expose one L2 latency per
+// split), the largest m2 is taken first, then the rescaled sums are added;
+// ex2.approx and lg2.approx move the result by about 1e-7 relative.
+__device__ __forceinline__ void chunk_row_lse(const ScoreArgs& a, const ItemTC& it, int row, int rows_c, int nsplit1,
+                                              float& nlse, int& tq) {
+  float l2 = INFINITY;
+  int t = -1;
+  if (row < rows_c) {
+    t = it.L - a.n + (it.qc * a.QC + row) % a.n;
+    const float2* src = a.p1part + pass1_item_index(a, it.r, it.g, it.qc, nsplit1) * a.QC + row;
+    const int64_t split_stride = (int64_t)a.NQC * a.QC;   // consecutive splits of one (g, qc)
+    float mm = -INFINITY, Z = 0.f;
+    for (int s0 = 0; s0 < nsplit1; s0 += 24) {
+      float2 pp[24];
+#pragma unroll
+      for (int k = 0; k < 24; ++k)
+        pp[k] = s0 + k < nsplit1 ? src[(s0 + k) * split_stride] : make_float2(-INFINITY, 0.f);
+      float mb = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 24; ++k)
+        if (pp[k].y > 0.f) mb = fmaxf(mb, pp[k].x);
+      if (mb > mm) {
+        Z = mm > -INFINITY ? Z * ex2_approx(mm - mb) : 0.f;
+        mm = mb;
+      }
+#pragma unroll
+      for (int k = 0; k < 24; ++k)
+        if (pp[k].y > 0.f) Z += pp[k].y * ex2_approx(pp[k].x - mm);
+    }
+    if (Z > 0.f && t >= 0) l2 = mm + lg2_approx(Z);
+    else t = -1;
+  }
+  nlse = -l2;
+  tq = t;
+}
+
 // With carried tables, one warp of pass 1's first CTA does what
 // describe_kernel does otherwise: it checks the device cu_seqlens against the
 // host's (a disagreement is reported; every kernel addresses the batch through

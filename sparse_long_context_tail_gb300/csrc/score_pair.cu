@@ -469,8 +469,8 @@ __device__ void pair_pass1_epilogue(const ScoreArgs& a, const PSmem& sm, const I
 __global__ void __launch_bounds__(kThreadsPair, 1)
     score_pass1_pair(const __grid_constant__ CUtensorMap tq_map, const __grid_constant__ CUtensorMap tk_map,
                      const __grid_constant__ ScoreArgs a) {
+  pdl_wait();      // then let pass 2 launch, which may read the queries and keys early
   pdl_trigger();
-  pdl_wait();
   extern __shared__ unsigned char smem_raw[];
   const int item = blockIdx.x >> 1;
   const uint32_t rank = cluster_ctarank();
@@ -582,8 +582,11 @@ __device__ void pair_pass2_epilogue(const ScoreArgs& a, const PSmem& sm, const I
 __global__ void __launch_bounds__(kThreadsPair, 1)
     score_pass2_pair(const __grid_constant__ CUtensorMap tq_map, const __grid_constant__ CUtensorMap tk_map,
                      const __grid_constant__ ScoreArgs a) {
+  // As in the single-CTA pass 2: with the descriptor in the parameters only
+  // the epilogue, which reads pass 1's partials, waits for pass 1.
+  const bool early = a.desc.R > 0;
   pdl_trigger();
-  pdl_wait();
+  if (!early) pdl_wait();
   extern __shared__ unsigned char smem_raw[];
   const int item = blockIdx.x >> 1;
   const uint32_t rank = cluster_ctarank();
@@ -607,40 +610,13 @@ __global__ void __launch_bounds__(kThreadsPair, 1)
       else pair_relay(a, sm, geo, ntiles);
     }
   } else {
+    if (early) pdl_wait();
     // -lse2 of every query column of the chunk (both CTAs' halves) from the
     // pass-1 partials of all key splits, stored negated; -inf marks columns
     // that do not exist.
     const int nsplit1 = ceil_div_dev(it.L, a.KS1);
-    for (int row = tid; row < qcols; row += kEpiThreads) {
-      float l2 = INFINITY;
-      int t = -1;
-      if (row < rows_c) {
-        t = it.L - a.n + (it.qc * a.QC + row) % a.n;
-        const float2* src = a.p1part + pass1_item_index(a, it.r, it.g, it.qc, nsplit1) * a.QC + row;
-        const int64_t split_stride = (int64_t)a.NQC * a.QC;
-        float mm = -INFINITY, Z = 0.f;
-        for (int s0 = 0; s0 < nsplit1; s0 += 16) {
-          float2 pp[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k)
-            pp[k] = s0 + k < nsplit1 ? src[(s0 + k) * split_stride] : make_float2(-INFINITY, 0.f);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            if (!(pp[k].y > 0.f)) continue;
-            if (pp[k].x > mm) {
-              Z = Z * exp2f(mm - pp[k].x) + pp[k].y;
-              mm = pp[k].x;
-            } else {
-              Z += pp[k].y * exp2f(pp[k].x - mm);
-            }
-          }
-        }
-        if (Z > 0.f && t >= 0) l2 = mm + log2f(Z);
-        else t = -1;
-      }
-      sm.nlse[row] = -l2;
-      sm.tq[row] = t;
-    }
+    for (int row = tid; row < qcols; row += kEpiThreads)
+      chunk_row_lse(a, it, row, rows_c, nsplit1, sm.nlse[row], sm.tq[row]);
     pepi_bar();
     pair_pass2_epilogue(a, sm, it, U, k0, k1, ntiles, tmem, warp, lane, rank);
   }

@@ -731,41 +731,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     // or positions before the request start).  The MMA runs meanwhile: the
     // first unit is not read before this is done.
     const int nsplit1 = ceil_div_dev(it.L, a.KS1);
-    for (int row = tid; row < qcols; row += kEpiThreads) {
-      float l2 = INFINITY;
-      int t = -1;
-      if (row < rows_c) {
-        t = it.L - a.n + (it.qc * a.QC + row) % a.n;
-        // One merge over the key splits, up to 24 partials loaded before any
-        // is used (a load feeding each step would expose one L2 latency per
-        // split while the MMA waits for the first unit's reader): the largest
-        // m first, then the rescaled sums.
-        const float2* src = a.p1part + pass1_item_index(a, it.r, it.g, it.qc, nsplit1) * a.QC + row;
-        const int64_t split_stride = (int64_t)a.NQC * a.QC;   // consecutive splits of one (g, qc)
-        float mm = -INFINITY, Z = 0.f;
-        for (int s0 = 0; s0 < nsplit1; s0 += 24) {
-          float2 pp[24];
-#pragma unroll
-          for (int k = 0; k < 24; ++k)
-            pp[k] = s0 + k < nsplit1 ? src[(s0 + k) * split_stride] : make_float2(-INFINITY, 0.f);
-          float mb = -INFINITY;
-#pragma unroll
-          for (int k = 0; k < 24; ++k)
-            if (pp[k].y > 0.f) mb = fmaxf(mb, pp[k].x);
-          if (mb > mm) {
-            Z = mm > -INFINITY ? Z * ex2_approx(mm - mb) : 0.f;
-            mm = mb;
-          }
-#pragma unroll
-          for (int k = 0; k < 24; ++k)
-            if (pp[k].y > 0.f) Z += pp[k].y * ex2_approx(pp[k].x - mm);
-        }
-        if (Z > 0.f && t >= 0) l2 = mm + lg2_approx(Z);
-        else t = -1;
-      }
-      sm.nlse[row] = -l2;
-      sm.tq[row] = t;
-    }
+    for (int row = tid; row < qcols; row += kEpiThreads)
+      chunk_row_lse(a, it, row, rows_c, nsplit1, sm.nlse[row], sm.tq[row]);
     epi_bar();
     if (geo.unit_cols == 256) pass2_epilogue<2>(a, sm, geo, it, U, k0, k1, ntiles, tmem, warp, lane);
     else pass2_epilogue<1>(a, sm, geo, it, U, k0, k1, ntiles, tmem, warp, lane);

@@ -198,8 +198,12 @@ __device__ void select_and_emit(const TailArgs& a, const DescView& dv, int r, co
 }
 
 __global__ void __launch_bounds__(kTailThreads) tail_kernel(const __grid_constant__ TailArgs a) {
+  // With the descriptor in the parameters the owned blocks' token ranges come
+  // from the parameters alone: worked out while pass 2's last CTAs finish,
+  // before the wait for pass 2's partial sums.
+  const bool early = a.desc.R > 0;
   pdl_trigger();
-  pdl_wait();
+  if (!early) pdl_wait();
   extern __shared__ unsigned char s_dyn[];
   __shared__ int s_bstart[kTailMaxBpc + 1];   // first packed token of each owned block, then the run's end
   __shared__ float s_inv[kTailMaxBpc];
@@ -210,6 +214,7 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const __grid_constan
   const DescView dv = tail_view(a);
   const int nb_total = dv.blk[s.R];   // 0 if the describe kernel rejected the descriptor
   if (nb_total == 0) {
+    if (early) pdl_wait();
     if (blockIdx.x == 0) finish_batch(a, dv, true);
     return;
   }
@@ -235,6 +240,7 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const __grid_constan
     s_nsel = 0;
     s_last = 0;
   }
+  if (early) pdl_wait();
   __syncthreads();
   const int tfirst = s_bstart[0], ntok = s_bstart[nown] - tfirst;
   float* s_val = reinterpret_cast<float*>(s_dyn);   // [ntok] token scores of the run
