@@ -16,9 +16,11 @@
 // every request its run touches (one atomic per request); the CTA that
 // completes a request runs that request's selection (select_core.cuh) with all
 // its threads, writes the request's keep bits, its kept count and the list of
-// its kept blocks with their output offsets, and counts the request done.  The CTA that completes the last request writes
-// the compacted batch offsets, the total, the keep-bit words shared by
-// neighbouring requests, and zero counts for empty requests.  Nothing waits:
+// its kept blocks with their output offsets, and counts the request done.  The
+// CTA that completes the last request writes the compacted batch offsets, the
+// total, the keep-bit words shared by neighbouring requests, and zero counts
+// for empty requests (a batch of one request needs none of that: its
+// selecting CTA writes every word and the offsets itself).  Nothing waits:
 // completion is detected with fenced atomics, so there is no spin anywhere.
 //
 // The per-token and per-block sums follow the same order as the separate
@@ -134,8 +136,9 @@ __device__ void finish_batch(const TailArgs& a, const DescView& dv, bool no_bloc
 
 // Selection of request r by the whole CTA, then its keep bits (whole words
 // inside the request by plain stores, the first and last word's bits to the
-// edge scratch), its count and its kept-token list.
-__device__ void select_and_emit(const TailArgs& a, const DescView& dv, int r, const SelectScratch& sc) {
+// edge scratch unless the batch is this one request), its count and its
+// kept-token list.  Returns the kept-token count.
+__device__ int select_and_emit(const TailArgs& a, const DescView& dv, int r, const SelectScratch& sc) {
   __shared__ int s_warp[kTailWarps], s_warpb[kTailWarps];
   const SelectArgs& s = a.s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -145,7 +148,7 @@ __device__ void select_and_emit(const TailArgs& a, const DescView& dv, int r, co
   const int w0 = tok0 >> 5, w1 = (tok0 + L - 1) >> 5;
   for (int w = w0 + tid; w <= w1; w += blockDim.x) {
     const uint32_t bits = request_word_bits(sc.keep, tok0, L, s.G, w);
-    const bool partial = (w * 32 < tok0) || (w * 32 + 32 > tok0 + L);
+    const bool partial = s.R > 1 && ((w * 32 < tok0) || (w * 32 + 32 > tok0 + L));
     if (!partial) {
       s.keep_bits[w] = bits;
     } else {   // read by the CTA that finishes the batch
@@ -195,6 +198,7 @@ __device__ void select_and_emit(const TailArgs& a, const DescView& dv, int r, co
   }
   if (tid == 0) s.kept_count[r] = kept;   // read by the CTA that finishes the batch
   __syncthreads();
+  return kept;
 }
 
 __global__ void __launch_bounds__(kTailThreads) tail_kernel(const __grid_constant__ TailArgs a) {
@@ -292,7 +296,18 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const __grid_constan
   const int nsel = s_nsel;
   if (nsel == 0) return;
   const SelectScratch sc = carve_select(s_dyn, a.nbp);
-  for (int k = 0; k < nsel; ++k) select_and_emit(a, dv, s_sel[k], sc);
+  int kept = 0;
+  for (int k = 0; k < nsel; ++k) kept = select_and_emit(a, dv, s_sel[k], sc);
+  if (s.R == 1) {
+    // One request: its words are all its own (written above), so the batch's
+    // offsets and total follow from its count with no further reads.
+    if (tid == 0 && a.cu_out) {
+      a.cu_out[0] = 0;
+      a.cu_out[1] = kept;
+      *a.total_kept = kept;
+    }
+    return;
+  }
   if (tid == 0) {
     // With one request (or this CTA completing all of them) nothing else is pending.
     if (nsel == a.nonempty || add_acq_rel(a.counters + s.R, nsel) + nsel == a.nonempty) s_last = 1;
@@ -303,17 +318,49 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const __grid_constan
 
 // The gather of the fused path: output row o belongs to the request r with
 // cu_out[r] <= o < cu_out[r+1]; its kept block is the last one of r's list
-// whose output offset is <= o - cu_out[r] (binary search; every lane does the
-// same loads), and its input row follows from the block's first token.  One
-// warp per output row, 16-byte vectors, eight in flight per lane; block 0
-// appends the drop-history record.
-__global__ void __launch_bounds__(256) gather_list_kernel(const __grid_constant__ GatherListArgs g) {
+// whose output offset is <= o - cu_out[r], and its input row follows from the
+// block's first token.  One warp per output row; block 0 appends the
+// drop-history record.
+//
+// Latency is the cost here (about one row per warp at the usual kept
+// fractions), so the dependent round trips are few: warp 0 of each CTA loads
+// the total, request 0's kept-block count and request 0's first 32 kept blocks
+// at once (its block range is known before the tail's results are), and a
+// row of request 0 with at most 32 kept blocks (every row of a single
+// request at those fractions) finds its block in shared memory.  Each lane
+// then loads all of its row's 16-byte vectors (up to 16, 8 KB a row) before
+// it stores any.
+constexpr int kGatherThreads = 256;
+constexpr int kGatherVec = 16;   // vectors per lane in flight
+
+__global__ void __launch_bounds__(kGatherThreads) gather_list_kernel(const __grid_constant__ GatherListArgs g) {
+  __shared__ int s_total, s_nblk0;
+  __shared__ int s_off0[32], s_blk0[32];
+  if (threadIdx.x == 0) {   // an empty batch: no rows
+    s_total = 0;
+    s_nblk0 = 0;
+  }
   pdl_trigger();
   pdl_wait();
   const CompactArgs& a = g.c;
   const DescView dv = gather_view(g);
-  const int total = min(*a.total_kept, a.T);
-  if (blockIdx.x == 0 && threadIdx.x == 0 && a.history) {
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32 && a.R > 0) {
+    const int base0 = dv.blk[0], nb0 = dv.blk[1] - base0;
+    int off = INT_MAX, blk = 0;
+    if (lane < nb0) {   // inside request 0's block range; entries past its count are unused
+      off = g.kept_off[base0 + lane];
+      blk = g.kept_blk[base0 + lane];
+    }
+    const int total = *a.total_kept, nblk0 = g.kept_nblk[0];
+    s_off0[lane] = off;
+    s_blk0[lane] = blk;
+    if (lane == 0) {
+      s_total = min(total, a.T);
+      s_nblk0 = nblk0;
+    }
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 32 && a.history) {
     bool full = false;
     for (int r = 0; r < a.R; ++r) full |= a.history_len[r] >= a.history_cap || a.history_len[r] < 0;
     if (full) {
@@ -328,22 +375,32 @@ __global__ void __launch_bounds__(256) gather_list_kernel(const __grid_constant_
       }
     }
   }
-  const int lane = threadIdx.x & 31;
+  __syncthreads();
+  const int total = s_total, nblk0 = s_nblk0;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
   const int64_t nvec = a.row_bytes / 16;
   for (int o = warp; o < total; o += nwarps) {
-    const int r = owner_of(a.cu_out, a.R, o);
-    const int j = o - a.cu_out[r];
+    const int r = a.R == 1 ? 0 : owner_of(a.cu_out, a.R, o);
+    const int j = r == 0 ? o : o - a.cu_out[r];
     const int base = dv.blk[r];
+    int lo = 0, n = r == 0 ? nblk0 : g.kept_nblk[r];
+    if (n <= 0) continue;   // never for a consistent batch
+    int kb = -1, koff = 0;
+    if (r == 0 && n <= 32) {
+      const int off = lane < n ? s_off0[lane] : INT_MAX;
+      const unsigned below = __ballot_sync(0xffffffffu, off <= j);   // lane 0 always: offset 0 <= j
+      if (!below) continue;   // never for a consistent batch
+      const int last = 31 - __clz(below);
+      kb = s_blk0[last];
+      koff = s_off0[last];
+      n = 1;
+    }
     // 32-way search: each lane probes one of 32 evenly spaced kept blocks and
     // the last probe at or below j narrows the range (one round for up to 32
     // kept blocks, two for up to 1024).  Each probe also loads its block's
     // index, so when the probes are single blocks the answer is already in a
-    // lane's registers: one dependent round trip less before the row's copy.
-    int lo = 0, n = g.kept_nblk[r];
-    if (n <= 0) continue;   // never for a consistent batch
-    int kb = -1, koff = 0;
+    // lane's registers.
     while (n > 1) {
       const int step = (n + 31) >> 5;
       const int at = lane * step;
@@ -373,15 +430,15 @@ __global__ void __launch_bounds__(256) gather_list_kernel(const __grid_constant_
     if (a.hidden_in) {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(a.hidden_in) + (int64_t)t * a.row_bytes);
       uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(a.hidden_out) + (int64_t)o * a.row_bytes);
-      int64_t v = lane;
-      for (; v + 224 < nvec; v += 256) {
-        uint4 x[8];
+      for (int64_t v0 = lane; v0 < nvec; v0 += 32 * kGatherVec) {
+        uint4 x[kGatherVec];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = __ldcs(src + v + 32 * u);
+        for (int u = 0; u < kGatherVec; ++u)
+          if (v0 + 32 * u < nvec) x[u] = __ldcs(src + v0 + 32 * u);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) __stcs(dst + v + 32 * u, x[u]);
+        for (int u = 0; u < kGatherVec; ++u)
+          if (v0 + 32 * u < nvec) __stcs(dst + v0 + 32 * u, x[u]);
       }
-      for (; v < nvec; v += 32) __stcs(dst + v, __ldcs(src + v));
     }
     if (lane == 1 && a.pos_in) a.pos_out[o] = a.pos_in[t];
     if (lane == 2 && a.slot_in) a.slot_out[o] = a.slot_in[t];
@@ -413,9 +470,13 @@ cudaError_t launch_tail(const TailArgs& a, cudaStream_t s, bool pdl) {
 }
 
 cudaError_t launch_gather_list(const GatherListArgs& a, cudaStream_t s, bool pdl) {
-  int blocks = (a.c.T + 7) / 8;
-  blocks = blocks < 1 ? 1 : (blocks > 8 * kPlanSMs ? 8 * kPlanSMs : blocks);
-  return launch_kernel(gather_list_kernel, blocks, 256, 0, s, pdl, a);
+  // At most one row per warp, and no more CTAs than fit on the GPU at once
+  // (two per SM at this kernel's register count), so the CTAs left without
+  // a row finish in the same wave as the others.
+  const int wpc = kGatherThreads / 32;
+  int blocks = (a.c.T + wpc - 1) / wpc;
+  blocks = blocks < 1 ? 1 : (blocks > 2 * kPlanSMs ? 2 * kPlanSMs : blocks);
+  return launch_kernel(gather_list_kernel, blocks, kGatherThreads, 0, s, pdl, a);
 }
 
 }  // namespace upf
