@@ -92,8 +92,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a,
   }
   const int kept = select_request(a.block_scores + b0, nb, L, a.G, a.top_p, a.sink_keep, a.tail_keep, sc, a.status);
   const int w0 = tok0 >> 5, w1 = (tok0 + L - 1) >> 5;
+  const int gshift = block_shift(a.G);
   for (int w = w0 + tid; w <= w1; w += blockDim.x) {
-    const uint32_t bits = request_word_bits(sc.keep, tok0, L, a.G, w);
+    const uint32_t bits = request_word_bits(sc.keep, tok0, L, a.G, gshift, w);
     const bool shared_word = (w * 32 < tok0) || (w * 32 + 32 > tok0 + L);
     if (shared_word) atomicOr(&a.keep_bits[w], bits);
     else a.keep_bits[w] = bits;

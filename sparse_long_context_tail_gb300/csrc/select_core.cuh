@@ -52,29 +52,47 @@ __device__ __forceinline__ SelectScratch carve_select(unsigned char* dyn, int nb
   return s;
 }
 
-// 2^e as a float, for e in [-126, 127].
-__device__ __forceinline__ float sel_pow2f(int e) { return __int_as_float((127 + e) << 23); }
-
 // Block masses as 48-bit fixed point relative to the largest block of the
-// request: m = floor(v * 2^(48 - ex)) with vmax = f * 2^ex, f in [0.5, 1), so
-// every m < 2^48 and a request's total (<= 16384 blocks) stays below 2^62.
-// The scaling is by powers of two only (two steps keep each factor normal).
+// request: m = floor(v * 2^sh), sh = 48 - ex with vmax = f * 2^ex, f in
+// [0.5, 1), so every m < 2^48 and a request's total (<= 16384 blocks) stays
+// below 2^62.  Exact, from the float's fields: v (>= 0, <= vmax) is
+// mant * 2^(e - 150) with e the biased exponent (1 for subnormals), so m is
+// mant shifted by e - 150 + sh (at most 25 to the left).
 __device__ __forceinline__ unsigned long long fixed_mass(float v, int sh) {
-  const int s1 = min(sh, 127);
-  return __float2ull_rz((v * sel_pow2f(s1)) * sel_pow2f(sh - s1));
+  const uint32_t b = __float_as_uint(v);
+  const int e = int(b >> 23);
+  const uint32_t mant = (b & 0x7FFFFFu) | (e ? 0x800000u : 0u);
+  const int s = (e ? e : 1) - 150 + sh;
+  if (s >= 0) return (unsigned long long)mant << s;
+  return s > -32 ? (unsigned long long)(mant >> -s) : 0ull;
 }
 
-template <typename T>
-__device__ __forceinline__ T sel_block_sum(T v, T* s_tmp) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if (lane == 0) s_tmp[warp] = v;
+// Cross-warp reductions of one value per warp (kSelWarps == 32: lane w reads
+// warp w's value), each one warp instruction in every warp, so no thread
+// walks the array.  Integer sums, maxima and ORs do not depend on the order.
+static_assert(kSelWarps == 32, "one per-warp value per lane");
+
+// Sum over the warp's lanes of v (each < 2^62, the sum < 2^64) in three
+// 21-bit parts, so no 32-bit part sum overflows.
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+  const uint32_t p0 = __reduce_add_sync(0xffffffffu, uint32_t(v & 0x1FFFFFull));
+  const uint32_t p1 = __reduce_add_sync(0xffffffffu, uint32_t((v >> 21) & 0x1FFFFFull));
+  const uint32_t p2 = __reduce_add_sync(0xffffffffu, uint32_t(v >> 42));
+  return (unsigned long long)p0 + ((unsigned long long)p1 << 21) + ((unsigned long long)p2 << 42);
+}
+
+// Sum of the values of the warps before this one.
+__device__ __forceinline__ int warps_before_sum(const int* s_w) {
+  const int lane = threadIdx.x & 31;
+  return __reduce_add_sync(0xffffffffu, lane < (int(threadIdx.x) >> 5) ? s_w[lane] : 0);
+}
+
+// The CTA's sum of v (the total < 2^62); every thread gets it.
+__device__ __forceinline__ unsigned long long sel_block_sum(unsigned long long v, unsigned long long* s_tmp) {
+  v = warp_sum_u64(v);
+  if ((threadIdx.x & 31) == 0) s_tmp[threadIdx.x >> 5] = v;
   __syncthreads();
-  T t = 0;
-  for (int w = 0; w < kSelWarps; ++w) t += s_tmp[w];   // fixed order
-  __syncthreads();
-  return t;
+  return warp_sum_u64(s_tmp[threadIdx.x & 31]);   // s_tmp is written again only after later barriers
 }
 
 // Mass histograms are kept as three 32-bit histograms of the masses' 16-bit
@@ -121,8 +139,9 @@ __device__ __forceinline__ void hist_add_aggregated(MassHist& h, uint32_t digit,
   }
 }
 
-// Selects the blocks of one request: block scores bs[0..nb) (global, any
-// state space the CTA can read), L tokens.  On return (after a barrier)
+// Selects the blocks of one request, called by every thread of a CTA of
+// exactly kSelThreads threads: block scores bs[0..nb) (global, any state
+// space the CTA can read), L tokens.  On return (after a barrier)
 // sc.keep[i] says whether block i is kept (top-p set or exempt) and the
 // kept-token count is returned to every thread.  A NaN, infinite or negative
 // score keeps the whole request and records UPF_ERR_NONFINITE.
@@ -132,7 +151,7 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
   __shared__ unsigned long long s_u64[kSelWarps];
   __shared__ float s_f[kSelWarps];
   __shared__ int s_i[kSelWarps];
-  __shared__ int s_digit, s_cnt;
+  __shared__ int s_digit;
   __shared__ unsigned long long s_above;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // Load, validate (finite and >= 0) and find the largest score.
@@ -153,13 +172,13 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
     s_i[warp] = bad;
   }
   __syncthreads();
-  vmax = 0.f;
-  bad = 0;
-  for (int w = 0; w < kSelWarps; ++w) {
-    vmax = fmaxf(vmax, s_f[w]);
-    bad |= s_i[w];
+  // Every per-warp maximum is a finite non-negative float unless `bad` is
+  // set (then vmax is not used), so its bit pattern orders like its value.
+  {
+    const uint32_t fb = __float_as_uint(s_f[lane]);
+    vmax = __uint_as_float(__reduce_max_sync(0xffffffffu, (fb & 0x80000000u) ? 0u : fb));
+    bad = int(__reduce_or_sync(0xffffffffu, uint32_t(s_i[lane])));
   }
-  if (tid == 0) s_cnt = 0;
   if (bad) {
     if (tid == 0) set_status(status, UPF_ERR_NONFINITE);
     for (int i = tid; i < nb; i += blockDim.x) sc.keep[i] = 1;
@@ -275,8 +294,7 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
       }
       if (lane == 31) s_i[warp] = incl;
       __syncthreads();
-      int before = incl - ties;
-      for (int ww = 0; ww < warp; ++ww) before += s_i[ww];
+      const int before = incl - ties + warps_before_sum(s_i);
       if (ties > 0) {
         // every tied block carries the same mass w > 0 (the boundary bucket reached the target)
         const unsigned long long need = target - above;
@@ -295,6 +313,7 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
   // tokens, each block by the thread that owns it in this loop.
   const int sink_hi = min(sink_keep, L);
   const int tail_lo = max(0, L - tail_keep);
+  __shared__ int s_cw[kSelWarps];
   int cnt = 0;
   for (int i = tid; i < nb; i += blockDim.x) {
     const int lo = i * G, hi = min(L, lo + G);
@@ -305,21 +324,22 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
     }
     if (kept) cnt += hi - lo;
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-  if (lane == 0 && cnt) atomicAdd(&s_cnt, cnt);
+  cnt = int(__reduce_add_sync(0xffffffffu, uint32_t(cnt)));
+  if (lane == 0) s_cw[warp] = cnt;
   __syncthreads();
-  return s_cnt;
+  return int(__reduce_add_sync(0xffffffffu, uint32_t(s_cw[lane])));
 }
 
 // Keep-bit word w of the packed tokens [tok0, tok0 + L) of a request whose
 // block flags are keep[]: bit (t % 32) set for kept tokens t of the request
-// in that word, 0 for tokens outside it.
-__device__ __forceinline__ uint32_t request_word_bits(const unsigned char* keep, int tok0, int L, int G, int w) {
+// in that word, 0 for tokens outside it.  gshift = log2(G) when G is a power
+// of two (the block of a token is then a shift), else -1.
+__device__ __forceinline__ uint32_t request_word_bits(const unsigned char* keep, int tok0, int L, int G, int gshift,
+                                                      int w) {
   uint32_t bits = 0;
   const int t_lo = max(tok0, w * 32), t_hi = min(tok0 + L, w * 32 + 32);
   for (int t = t_lo; t < t_hi;) {   // walk the blocks that overlap this word's tokens
-    const int blk = (t - tok0) / G;
+    const int blk = gshift >= 0 ? (t - tok0) >> gshift : (t - tok0) / G;
     const int t_end = min(t_hi, tok0 + (blk + 1) * G);
     if (keep[blk]) {
       const int len = t_end - t;
@@ -328,6 +348,13 @@ __device__ __forceinline__ uint32_t request_word_bits(const unsigned char* keep,
     t = t_end;
   }
   return bits;
+}
+
+__host__ __device__ __forceinline__ int block_shift(int G) {
+  if (G <= 0 || (G & (G - 1))) return -1;
+  int k = 0;
+  while ((1 << k) < G) ++k;
+  return k;
 }
 
 }  // namespace upf

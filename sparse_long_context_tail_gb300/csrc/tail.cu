@@ -121,8 +121,7 @@ __device__ void finish_batch(const TailArgs& a, const DescView& dv, bool no_bloc
     }
     if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
-    int before = s_carry;
-    for (int w = 0; w < warp; ++w) before += s_warp[w];
+    const int before = s_carry + warps_before_sum(s_warp);
     if (r < s.R) a.cu_out[r] = before + incl - v;
     __syncthreads();
     if (tid == blockDim.x - 1) s_carry = before + incl;
@@ -146,8 +145,9 @@ __device__ int select_and_emit(const TailArgs& a, const DescView& dv, int r, con
   const int tok0 = dv.cu[r], L = dv.cu[r + 1] - tok0;
   const int kept = select_request(s.block_scores + b0, nb, L, s.G, s.top_p, s.sink_keep, s.tail_keep, sc, s.status);
   const int w0 = tok0 >> 5, w1 = (tok0 + L - 1) >> 5;
+  const int gshift = block_shift(s.G);
   for (int w = w0 + tid; w <= w1; w += blockDim.x) {
-    const uint32_t bits = request_word_bits(sc.keep, tok0, L, s.G, w);
+    const uint32_t bits = request_word_bits(sc.keep, tok0, L, s.G, gshift, w);
     const bool partial = s.R > 1 && ((w * 32 < tok0) || (w * 32 + 32 > tok0 + L));
     if (!partial) {
       s.keep_bits[w] = bits;
@@ -182,11 +182,7 @@ __device__ int select_and_emit(const TailArgs& a, const DescView& dv, int r, con
       s_warpb[warp] = inclb;
     }
     __syncthreads();
-    int run = incl - mine, runb = inclb - mineb;
-    for (int w = 0; w < warp; ++w) {
-      run += s_warp[w];
-      runb += s_warpb[w];
-    }
+    int run = incl - mine + warps_before_sum(s_warp), runb = inclb - mineb + warps_before_sum(s_warpb);
     for (int i = i0; i < i1; ++i)
       if (sc.keep[i]) {
         a.kept_blk[b0 + runb] = i;
