@@ -67,6 +67,31 @@ __device__ __forceinline__ unsigned long long fixed_mass(float v, int sh) {
   return s > -32 ? (unsigned long long)(mant >> -s) : 0ull;
 }
 
+// The smallest integer >= top_p * total, exactly, for top_p in [0, 1] and
+// total < 2^62: top_p = mp / 2^k with mp the 24-bit significand, so the
+// answer is the 88-bit product mp * total shifted right by k, rounded up.
+// Integer arithmetic throughout (no double precision, which is slow here).
+__device__ __forceinline__ unsigned long long mass_target(float top_p, unsigned long long total) {
+  const uint32_t b = __float_as_uint(top_p);
+  const int e = int(b >> 23) & 0xFF;
+  const unsigned long long mp = (b & 0x7FFFFFu) | (e ? 0x800000u : 0u);
+  const int k = 150 - (e ? e : 1);   // >= 23 for top_p <= 1
+  const unsigned long long lo = total * mp, hi = __umul64hi(total, mp);
+  unsigned long long q;
+  bool rem;
+  if (k < 64) {
+    q = (hi << (64 - k)) | (lo >> k);
+    rem = (lo & ((1ull << k) - 1ull)) != 0;
+  } else if (k < 128) {
+    q = k == 64 ? hi : hi >> (k - 64);
+    rem = lo != 0 || (k > 64 && (hi & ((1ull << (k - 64)) - 1ull)) != 0);
+  } else {
+    q = 0;
+    rem = lo != 0 || hi != 0;
+  }
+  return q + (rem ? 1ull : 0ull);
+}
+
 // Cross-warp reductions of one value per warp (kSelWarps == 32: lane w reads
 // warp w's value), each one warp instruction in every warp, so no thread
 // walks the array.  Integer sums, maxima and ORs do not depend on the order.
@@ -97,10 +122,13 @@ __device__ __forceinline__ unsigned long long sel_block_sum(unsigned long long v
 
 // Mass histograms are kept as three 32-bit histograms of the masses' 16-bit
 // parts (native 32-bit shared atomics; a bucket's part sum stays below
-// 16384 * 2^16 = 2^30), combined when the buckets are scanned.
+// 16384 * 2^16 = 2^30), combined when the buckets are scanned, beside the
+// buckets' block counts.
 struct MassHist {
   uint32_t p[3][256];
+  uint32_t c[256];
 };
+constexpr int kHistWords = 4 * 256;
 
 __device__ __forceinline__ unsigned long long hist_mass(const MassHist& h, int d) {
   return (unsigned long long)h.p[0][d] + ((unsigned long long)h.p[1][d] << 16) + ((unsigned long long)h.p[2][d] << 32);
@@ -129,6 +157,7 @@ __device__ __forceinline__ void hist_add_aggregated(MassHist& h, uint32_t digit,
       atomicAdd(&h.p[0][d], s0);
       atomicAdd(&h.p[1][d], s1);
       atomicAdd(&h.p[2][d], s2);
+      atomicAdd(&h.c[d], uint32_t(__popc(group)));
     }
     pending &= ~group;
   }
@@ -136,7 +165,29 @@ __device__ __forceinline__ void hist_add_aggregated(MassHist& h, uint32_t digit,
     atomicAdd(&h.p[0][digit], m0);
     atomicAdd(&h.p[1][digit], m1);
     atomicAdd(&h.p[2][digit], m2);
+    atomicAdd(&h.c[digit], 1u);
   }
+}
+
+// Ranks candidate blocks by counting: candidate t (block cand[t], or block t
+// without a list) is kept when the mass ranked before it (score desc, index
+// asc) is below the target: `above` (every block ranked before all the
+// candidates) plus the candidates ranked before it.  Thread t handles
+// candidate t (nc <= kCountSel <= the CTA's threads).
+template <bool kList>
+__device__ __forceinline__ void rank_candidates(const SelectScratch& sc, const int* cand, int nc,
+                                                unsigned long long above, unsigned long long target) {
+  const int t = threadIdx.x;
+  if (t >= nc) return;
+  const int i = kList ? cand[t] : t;
+  const unsigned long long ki = ((unsigned long long)sc.bits[i] << 32) | (0xFFFFFFFFu - uint32_t(i));
+  unsigned long long before = above;
+  for (int c = 0; c < nc; ++c) {
+    const int j = kList ? cand[c] : c;
+    const unsigned long long kj = ((unsigned long long)sc.bits[j] << 32) | (0xFFFFFFFFu - uint32_t(j));
+    if (kj > ki) before += sc.m[j];
+  }
+  if (before < target) sc.keep[i] = 1;
 }
 
 // Selects the blocks of one request, called by every thread of a CTA of
@@ -151,7 +202,8 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
   __shared__ unsigned long long s_u64[kSelWarps];
   __shared__ float s_f[kSelWarps];
   __shared__ int s_i[kSelWarps];
-  __shared__ int s_digit;
+  __shared__ int s_digit, s_count, s_ncand;
+  __shared__ int s_cand[kCountSel];
   __shared__ unsigned long long s_above;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // Load, validate (finite and >= 0) and find the largest score.
@@ -192,28 +244,20 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
       sc.m[i] = m;
       part += m;
     }
-    for (int d = tid; d < 3 * 256; d += blockDim.x) (&h_mass[0].p[0][0])[d] = 0;   // ordered by the barriers in the sum
+    for (int d = tid; d < kHistWords; d += blockDim.x) (&h_mass[0].p[0][0])[d] = 0;   // ordered by the barrier in the sum
     const unsigned long long total = sel_block_sum(part, s_u64);
     // Mass the selected prefix must reach: the smallest integer >= top_p * total.
-    const unsigned long long target = (unsigned long long)ceil((double)top_p * (double)total);
+    const unsigned long long target = mass_target(top_p, total);
     if (target > 0 && nb <= kCountSel) {
-      // Small request: block i's thread adds the masses of every block ranked
-      // before it (score desc, index asc) and keeps i while that sum is below
-      // the target: the radix select's set, without its rounds and barriers.
-      if (tid < nb) {
-        const unsigned long long ki = ((unsigned long long)sc.bits[tid] << 32) | (0xFFFFFFFFu - uint32_t(tid));
-        unsigned long long before = 0;
-        for (int j = 0; j < nb; ++j) {
-          const unsigned long long kj = ((unsigned long long)sc.bits[j] << 32) | (0xFFFFFFFFu - uint32_t(j));
-          if (kj > ki) before += sc.m[j];
-        }
-        if (before < target) sc.keep[tid] = 1;
-      }
+      // Small request: every block is a candidate, ranked by counting (the
+      // radix select's set, without its rounds and barriers).
+      rank_candidates<false>(sc, nullptr, nb, 0ull, target);
     } else if (target > 0) {
       uint32_t prefix = 0, pmask = 0;
       unsigned long long above = 0;   // mass of blocks ranked strictly before the candidates
       const int nb_pad = (nb + 31) & ~31;   // whole warps take part in the aggregation
       int cur = 0;
+      bool few = false;   // the boundary bucket holds at most kCountSel blocks
       for (int shift = 24; shift >= 0; shift -= 8, cur ^= 1) {
         MassHist& hist = h_mass[cur];
         for (int i = tid; i < nb_pad; i += blockDim.x) {
@@ -259,52 +303,84 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
             }
             s_digit = dsel;
             s_above = run;
+            s_count = int(hist.c[dsel]);
           }
-        } else if (tid < 32 + 3 * 256) {
-          (&h_mass[cur ^ 1].p[0][0])[tid - 32] = 0;   // the next round's histogram
+        } else {
+          for (int d = tid - 32; d < kHistWords; d += blockDim.x - 32)
+            (&h_mass[cur ^ 1].p[0][0])[d] = 0;   // the next round's histogram
+          if (tid == 32) s_ncand = 0;
         }
         __syncthreads();
         prefix |= uint32_t(s_digit) << shift;
         pmask |= 255u << shift;
         above = s_above;
-        // s_digit / s_above are rewritten only after the next round's first
-        // barrier, which every thread reaches after reading them here.
-      }
-      // prefix = bits of the boundary score v*.  Blocks above it are in; the
-      // tied ones (equal scores) enter in index order until the mass suffices.
-      // Thread t owns the contiguous index range [t*per, (t+1)*per).
-      const int per = (nb + blockDim.x - 1) / blockDim.x;
-      const int i0 = min(nb, tid * per), i1 = min(nb, i0 + per);
-      int ties = 0;
-      unsigned long long w = 0;
-      for (int i = i0; i < i1; ++i) {
-        const uint32_t b = sc.bits[i];
-        if (b > prefix) sc.keep[i] = 1;
-        else if (b == prefix) {
-          ++ties;
-          w = sc.m[i];
+        // s_digit / s_above / s_count are rewritten only after the next
+        // round's first barrier, which every thread reaches after reading
+        // them here.
+        if (s_count <= kCountSel) {
+          few = true;
+          break;
         }
       }
-      // exclusive scan of tie counts in index order
-      int incl = ties;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      if (lane == 31) s_i[warp] = incl;
-      __syncthreads();
-      const int before = incl - ties + warps_before_sum(s_i);
-      if (ties > 0) {
-        // every tied block carries the same mass w > 0 (the boundary bucket reached the target)
-        const unsigned long long need = target - above;
-        const unsigned long long take = w > 0 ? (need + w - 1) / w : 0;
-        int rank = before;
-        for (int i = i0; i < i1; ++i)
-          if (sc.bits[i] == prefix) {
-            if ((unsigned long long)rank < take) sc.keep[i] = 1;
-            ++rank;
+      if (few) {
+        // Blocks above the boundary bucket are in; the bucket's blocks are
+        // listed (in any order) and ranked by counting.  The same set as
+        // finishing the rounds and taking ties in index order.
+        for (int i = tid; i < nb_pad; i += blockDim.x) {
+          bool cand = false;
+          if (i < nb) {
+            const uint32_t bm = sc.bits[i] & pmask;
+            if (bm > prefix) sc.keep[i] = 1;
+            cand = bm == prefix;
           }
+          const unsigned bal = __ballot_sync(0xffffffffu, cand);
+          if (bal) {
+            int pos = 0;
+            if (lane == 0) pos = atomicAdd(&s_ncand, __popc(bal));
+            pos = __shfl_sync(0xffffffffu, pos, 0) + __popc(bal & ((1u << lane) - 1u));
+            if (cand && pos < kCountSel) s_cand[pos] = i;
+          }
+        }
+        __syncthreads();
+        rank_candidates<true>(sc, s_cand, min(s_ncand, kCountSel), above, target);
+      } else {
+        // prefix = bits of the boundary score v*.  Blocks above it are in; the
+        // tied ones (equal scores) enter in index order until the mass suffices.
+        // Thread t owns the contiguous index range [t*per, (t+1)*per).
+        const int per = (nb + blockDim.x - 1) / blockDim.x;
+        const int i0 = min(nb, tid * per), i1 = min(nb, i0 + per);
+        int ties = 0;
+        unsigned long long w = 0;
+        for (int i = i0; i < i1; ++i) {
+          const uint32_t b = sc.bits[i];
+          if (b > prefix) sc.keep[i] = 1;
+          else if (b == prefix) {
+            ++ties;
+            w = sc.m[i];
+          }
+        }
+        // exclusive scan of tie counts in index order
+        int incl = ties;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        if (lane == 31) s_i[warp] = incl;
+        __syncthreads();
+        const int before = incl - ties + warps_before_sum(s_i);
+        if (ties > 0) {
+          // every tied block carries the same mass w > 0 (the boundary bucket reached the target)
+          const unsigned long long need = target - above;   // > 0: the boundary bucket is needed
+          // Usually one tied block suffices (need <= w); the division is for the rest.
+          const unsigned long long take = need <= w ? 1ull : (w > 0 ? (need + w - 1) / w : 0ull);
+          int rank = before;
+          for (int i = i0; i < i1; ++i)
+            if (sc.bits[i] == prefix) {
+              if ((unsigned long long)rank < take) sc.keep[i] = 1;
+              ++rank;
+            }
+        }
       }
     }
   }
@@ -336,6 +412,12 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
 // of two (the block of a token is then a shift), else -1.
 __device__ __forceinline__ uint32_t request_word_bits(const unsigned char* keep, int tok0, int L, int G, int gshift,
                                                       int w) {
+  if (gshift >= 5 && (tok0 & 31) == 0) {
+    // Blocks are whole words: the word's tokens share one block (the last
+    // word of the request may hold fewer than 32 of its tokens).
+    const int t = w * 32, n = min(32, tok0 + L - t);
+    return keep[(t - tok0) >> gshift] ? (n >= 32 ? 0xffffffffu : ((1u << n) - 1u)) : 0u;
+  }
   uint32_t bits = 0;
   const int t_lo = max(tok0, w * 32), t_hi = min(tok0 + L, w * 32 + 32);
   for (int t = t_lo; t < t_hi;) {   // walk the blocks that overlap this word's tokens

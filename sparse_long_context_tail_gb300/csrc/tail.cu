@@ -138,7 +138,7 @@ __device__ void finish_batch(const TailArgs& a, const DescView& dv, bool no_bloc
 // edge scratch unless the batch is this one request), its count and its
 // kept-token list.  Returns the kept-token count.
 __device__ int select_and_emit(const TailArgs& a, const DescView& dv, int r, const SelectScratch& sc) {
-  __shared__ int s_warp[kTailWarps], s_warpb[kTailWarps];
+  __shared__ int s_warpb[kTailWarps];
   const SelectArgs& s = a.s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b0 = dv.blk[r], nb = dv.blk[r + 1] - b0;
@@ -157,37 +157,27 @@ __device__ int select_and_emit(const TailArgs& a, const DescView& dv, int r, con
   }
   if (a.kept_blk) {
     // The kept blocks in order with their output offsets inside the request
-    // (exclusive prefix of kept block sizes); thread t owns the contiguous
-    // blocks [t*per, (t+1)*per).  The gather expands them to token rows.
+    // (every block but the request's last holds G tokens, so a kept block's
+    // offset is G times the number of kept blocks before it); thread t owns
+    // the contiguous blocks [t*per, (t+1)*per).  The gather expands them to
+    // token rows.
     const int per = (nb + blockDim.x - 1) / blockDim.x;
     const int i0 = min(nb, tid * per), i1 = min(nb, i0 + per);
-    int mine = 0, mineb = 0;
-    for (int i = i0; i < i1; ++i)
-      if (sc.keep[i]) {
-        mine += min(L, (i + 1) * s.G) - i * s.G;
-        ++mineb;
-      }
-    int incl = mine, inclb = mineb;
+    int mineb = 0;
+    for (int i = i0; i < i1; ++i) mineb += sc.keep[i] ? 1 : 0;
+    int inclb = mineb;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
       const int tb = __shfl_up_sync(0xffffffffu, inclb, o);
-      if (lane >= o) {
-        incl += t;
-        inclb += tb;
-      }
+      if (lane >= o) inclb += tb;
     }
-    if (lane == 31) {
-      s_warp[warp] = incl;
-      s_warpb[warp] = inclb;
-    }
+    if (lane == 31) s_warpb[warp] = inclb;
     __syncthreads();
-    int run = incl - mine + warps_before_sum(s_warp), runb = inclb - mineb + warps_before_sum(s_warpb);
+    int runb = inclb - mineb + warps_before_sum(s_warpb);
     for (int i = i0; i < i1; ++i)
       if (sc.keep[i]) {
         a.kept_blk[b0 + runb] = i;
-        a.kept_off[b0 + runb] = run;
-        run += min(L, (i + 1) * s.G) - i * s.G;
+        a.kept_off[b0 + runb] = runb * s.G;
         ++runb;
       }
     if (tid == blockDim.x - 1) a.kept_nblk[r] = runb;

@@ -514,6 +514,31 @@ def test_select_ties_take_lower_blocks_first(sel):
         np.testing.assert_array_equal(mask, want)
 
 
+def test_select_boundary_bucket_small_after_each_round(sel):
+    """Score sets whose boundary bucket drops to at most 256 blocks after the
+    first, second, third or fourth 8-bit round of the radix select (and one
+    where it never does: over 256 equal scores), against the oracle's rule.
+    One token per block and scores exact in float32, so the block means are
+    the scores themselves."""
+    rng = np.random.default_rng(11)
+    nb = 2000
+    cases = [
+        (rng.exponential(1.0, nb) ** 4).astype(np.float32).astype(np.float64),   # exponents differ: first round
+        1.0 + rng.integers(0, 128, nb) * 2.0 ** -7,          # bits 16-22 differ: second round
+        1.5 + rng.integers(0, 512, nb) * 2.0 ** -16,         # bits 7-15 differ: third round
+        1.5 + rng.integers(0, 256, nb) * 2.0 ** -23,         # low byte differs: fourth round
+        np.array([1.0, 2.0, 3.0, 4.0])[rng.integers(0, 4, nb)],   # ~500 equal scores per value
+    ]
+    for vals in cases:
+        scores = vals.astype(np.float32)
+        assert np.array_equal(scores.astype(np.float64), vals)   # exact in float32
+        for top_p in (0.3, 0.9, 0.99):
+            status, mask, bs, cnt = _select_only(sel, scores, [0, nb], 1, top_p, sink=0, tail=0)
+            assert status == 0
+            want = oracle.select(scores.astype(np.float64), [0, nb], 1, top_p, 0, 0)["mask"]
+            np.testing.assert_array_equal(mask, want)
+
+
 def test_select_rejects_negative_scores(sel):
     scores = np.full(2000, 1.0 / 2000, dtype=np.float32)
     scores[768:832] = -1e-3          # block 12 has a negative mean
