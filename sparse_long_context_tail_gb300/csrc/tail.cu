@@ -413,6 +413,10 @@ __global__ void __launch_bounds__(kGatherThreads) gather_list_kernel(const __gri
     const int t = dv.cu[r] + kb * g.G + (j - koff);
     if (t < dv.cu[r] || t >= dv.cu[r + 1] || t >= a.T) continue;   // never for a consistent batch
     if (lane == 0 && a.kept_index) a.kept_index[o] = t;
+    // The row's position and slot load with the row itself (lanes 1 and 2).
+    int64_t side = 0;
+    if (lane == 1 && a.pos_in) side = a.pos_in[t];
+    if (lane == 2 && a.slot_in) side = a.slot_in[t];
     if (a.hidden_in) {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(a.hidden_in) + (int64_t)t * a.row_bytes);
       uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(a.hidden_out) + (int64_t)o * a.row_bytes);
@@ -426,8 +430,8 @@ __global__ void __launch_bounds__(kGatherThreads) gather_list_kernel(const __gri
           if (v0 + 32 * u < nvec) __stcs(dst + v0 + 32 * u, x[u]);
       }
     }
-    if (lane == 1 && a.pos_in) a.pos_out[o] = a.pos_in[t];
-    if (lane == 2 && a.slot_in) a.slot_out[o] = a.slot_in[t];
+    if (lane == 1 && a.pos_in) a.pos_out[o] = side;
+    if (lane == 2 && a.slot_in) a.slot_out[o] = side;
   }
 }
 
