@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(256) block_means_kernel(const SelectArgs a) {
 // total (select_core.cuh), then the keep bits of its tokens: interior words by
 // plain stores, the two words it may share with its neighbours by atomicOr
 // (block_means_kernel cleared them).
-__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelectArgs a, int nbp) {
+__global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelectArgs a, int nbp) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ unsigned char s_dyn[];

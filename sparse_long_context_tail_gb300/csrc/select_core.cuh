@@ -204,7 +204,7 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
   __shared__ int s_i[kSelWarps];
   __shared__ int s_digit, s_count, s_ncand;
   __shared__ int s_cand[kCountSel];
-  __shared__ unsigned long long s_above;
+  __shared__ unsigned long long s_above, s_wtot[8];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // Load, validate (finite and >= 0) and find the largest score.
   float vmax = 0.f;
@@ -216,6 +216,7 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
     vmax = fmaxf(vmax, v);
     sc.keep[i] = 0;
   }
+  for (int d = tid; d < kHistWords; d += blockDim.x) (&h_mass[0].p[0][0])[d] = 0;   // the first round's histogram
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
   bad = __any_sync(0xffffffffu, bad);
@@ -244,15 +245,17 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
       sc.m[i] = m;
       part += m;
     }
-    for (int d = tid; d < kHistWords; d += blockDim.x) (&h_mass[0].p[0][0])[d] = 0;   // ordered by the barrier in the sum
-    const unsigned long long total = sel_block_sum(part, s_u64);
-    // Mass the selected prefix must reach: the smallest integer >= top_p * total.
-    const unsigned long long target = mass_target(top_p, total);
-    if (target > 0 && nb <= kCountSel) {
+    // Mass the selected prefix must reach: the smallest integer >= top_p *
+    // total (zero: no block by top-p).
+    unsigned long long target = 0;
+    if (nb <= kCountSel) {
       // Small request: every block is a candidate, ranked by counting (the
       // radix select's set, without its rounds and barriers).
-      rank_candidates<false>(sc, nullptr, nb, 0ull, target);
-    } else if (target > 0) {
+      target = mass_target(top_p, sel_block_sum(part, s_u64));
+      if (target > 0) rank_candidates<false>(sc, nullptr, nb, 0ull, target);
+    } else {
+      // The total comes out of the first round's bucket scan (every block is
+      // in that round's histogram).
       uint32_t prefix = 0, pmask = 0;
       unsigned long long above = 0;   // mass of blocks ranked strictly before the candidates
       const int nb_pad = (nb + 31) & ~31;   // whole warps take part in the aggregation
@@ -273,50 +276,47 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
           hist_add_aggregated(hist, digit, m);
         }
         __syncthreads();
-        if (warp == 0) {
-          // Buckets from the highest digit down; lane l owns digits 255-8l .. 248-8l.
-          unsigned long long loc[8], lsum = 0;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            loc[j] = hist_mass(hist, 255 - 8 * lane - j);
-            lsum += loc[j];
-          }
-          unsigned long long incl = lsum;
+        // Warps 0-7 scan the buckets from the highest digit down, 32 each
+        // (lane l of warp w holds digit 255 - 32 w - l); the others clear the
+        // next round's histogram.
+        const int dg = 255 - 32 * warp - lane;
+        unsigned long long mass = 0, incl = 0;
+        if (warp < 8) {
+          mass = hist_mass(hist, dg);
+          incl = mass;
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
             const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += t;
           }
-          const unsigned long long base = above + incl - lsum;   // mass before this lane's digits
-          const bool hit = base + lsum >= target && base < target;
-          const unsigned int who = __ballot_sync(0xffffffffu, hit);
-          const int src = who ? __ffs(who) - 1 : 31;
-          if (lane == src) {
-            unsigned long long run = base;
-            int dsel = 255 - 8 * lane - 7;
-            for (int j = 0; j < 8; ++j) {
-              if (run + loc[j] >= target) {
-                dsel = 255 - 8 * lane - j;
-                break;
-              }
-              run += loc[j];
-            }
-            s_digit = dsel;
-            s_above = run;
-            s_count = int(hist.c[dsel]);
-          }
+          if (lane == 31) s_wtot[warp] = incl;
         } else {
-          for (int d = tid - 32; d < kHistWords; d += blockDim.x - 32)
-            (&h_mass[cur ^ 1].p[0][0])[d] = 0;   // the next round's histogram
-          if (tid == 32) s_ncand = 0;
+          for (int d = tid - 256; d < kHistWords; d += blockDim.x - 256)
+            (&h_mass[cur ^ 1].p[0][0])[d] = 0;
+          if (tid == 256) s_ncand = 0;
+        }
+        __syncthreads();
+        if (shift == 24) {
+          target = mass_target(top_p, warp_sum_u64(lane < 8 ? s_wtot[lane] : 0ull));
+          if (target == 0) break;   // the same in every thread
+        }
+        if (warp < 8) {
+          // Mass before this digit; exactly one digit starts below the target
+          // and reaches it (the prefix bucket reaches it).
+          const unsigned long long base = above + warp_sum_u64(lane < warp ? s_wtot[lane] : 0ull) + incl - mass;
+          if (base < target && base + mass >= target) {
+            s_digit = dg;
+            s_above = base;
+            s_count = int(hist.c[dg]);
+          }
         }
         __syncthreads();
         prefix |= uint32_t(s_digit) << shift;
         pmask |= 255u << shift;
         above = s_above;
-        // s_digit / s_above / s_count are rewritten only after the next
-        // round's first barrier, which every thread reaches after reading
-        // them here.
+        // s_wtot, s_digit, s_above and s_count are rewritten only after the
+        // next round's first barrier, which every thread reaches after
+        // reading them here.
         if (s_count <= kCountSel) {
           few = true;
           break;
@@ -343,7 +343,7 @@ static __device__ int select_request(const float* bs, int nb, int L, int G, floa
         }
         __syncthreads();
         rank_candidates<true>(sc, s_cand, min(s_ncand, kCountSel), above, target);
-      } else {
+      } else if (target > 0) {
         // prefix = bits of the boundary score v*.  Blocks above it are in; the
         // tied ones (equal scores) enter in index order until the mass suffices.
         // Thread t owns the contiguous index range [t*per, (t+1)*per).

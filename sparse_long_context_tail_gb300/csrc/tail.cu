@@ -187,7 +187,7 @@ __device__ int select_and_emit(const TailArgs& a, const DescView& dv, int r, con
   return kept;
 }
 
-__global__ void __launch_bounds__(kTailThreads) tail_kernel(const __grid_constant__ TailArgs a) {
+__global__ void __launch_bounds__(kTailThreads, 1) tail_kernel(const __grid_constant__ TailArgs a) {
   // With the descriptor in the parameters the owned blocks' token ranges come
   // from the parameters alone: worked out while pass 2's last CTAs finish,
   // before the wait for pass 2's partial sums.
@@ -305,7 +305,8 @@ __global__ void __launch_bounds__(kTailThreads) tail_kernel(const __grid_constan
 // The gather of the fused path: output row o belongs to the request r with
 // cu_out[r] <= o < cu_out[r+1]; its kept block is the last one of r's list
 // whose output offset is <= o - cu_out[r], and its input row follows from the
-// block's first token.  One warp per output row; block 0 appends the
+// block's first token.  One warp per output row (two, each copying a
+// part, when there are fewer rows than warps); block 0 appends the
 // drop-history record.
 //
 // Latency is the cost here (about one row per warp at the usual kept
@@ -366,7 +367,12 @@ __global__ void __launch_bounds__(kGatherThreads) gather_list_kernel(const __gri
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
   const int64_t nvec = a.row_bytes / 16;
-  for (int o = warp; o < total; o += nwarps) {
+  // With fewer rows than warps, two warps share a row (each copies a
+  // contiguous part), so the copies spread over more SMs.
+  const int wpr = total > 0 ? max(1, min(2, nwarps / total)) : 1;
+  const int64_t part_vec = ((nvec + wpr - 1) / wpr + 31) & ~int64_t(31);
+  for (int wi = warp; wi < total * wpr; wi += nwarps) {
+    const int o = wi / wpr, part = wi - o * wpr;
     const int r = a.R == 1 ? 0 : owner_of(a.cu_out, a.R, o);
     const int j = r == 0 ? o : o - a.cu_out[r];
     const int base = dv.blk[r];
@@ -412,26 +418,28 @@ __global__ void __launch_bounds__(kGatherThreads) gather_list_kernel(const __gri
     }
     const int t = dv.cu[r] + kb * g.G + (j - koff);
     if (t < dv.cu[r] || t >= dv.cu[r + 1] || t >= a.T) continue;   // never for a consistent batch
-    if (lane == 0 && a.kept_index) a.kept_index[o] = t;
+    const bool first = part == 0;   // the part that writes the row's index, position and slot
+    if (first && lane == 0 && a.kept_index) a.kept_index[o] = t;
     // The row's position and slot load with the row itself (lanes 1 and 2).
     int64_t side = 0;
-    if (lane == 1 && a.pos_in) side = a.pos_in[t];
-    if (lane == 2 && a.slot_in) side = a.slot_in[t];
+    if (first && lane == 1 && a.pos_in) side = a.pos_in[t];
+    if (first && lane == 2 && a.slot_in) side = a.slot_in[t];
     if (a.hidden_in) {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(a.hidden_in) + (int64_t)t * a.row_bytes);
       uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(a.hidden_out) + (int64_t)o * a.row_bytes);
-      for (int64_t v0 = lane; v0 < nvec; v0 += 32 * kGatherVec) {
+      const int64_t v_end = min(nvec, (part + 1) * part_vec);
+      for (int64_t v0 = part * part_vec + lane; v0 < v_end; v0 += 32 * kGatherVec) {
         uint4 x[kGatherVec];
 #pragma unroll
         for (int u = 0; u < kGatherVec; ++u)
-          if (v0 + 32 * u < nvec) x[u] = __ldcs(src + v0 + 32 * u);
+          if (v0 + 32 * u < v_end) x[u] = __ldcs(src + v0 + 32 * u);
 #pragma unroll
         for (int u = 0; u < kGatherVec; ++u)
-          if (v0 + 32 * u < nvec) __stcs(dst + v0 + 32 * u, x[u]);
+          if (v0 + 32 * u < v_end) __stcs(dst + v0 + 32 * u, x[u]);
       }
     }
-    if (lane == 1 && a.pos_in) a.pos_out[o] = side;
-    if (lane == 2 && a.slot_in) a.slot_out[o] = side;
+    if (first && lane == 1 && a.pos_in) a.pos_out[o] = side;
+    if (first && lane == 2 && a.slot_in) a.slot_out[o] = side;
   }
 }
 
