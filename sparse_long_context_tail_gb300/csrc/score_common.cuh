@@ -88,14 +88,30 @@ __device__ __forceinline__ int64_t pass1_item_index(const ScoreArgs& a, int r, i
 // any is used (a load feeding each step would expose one L2 latency per
 // split), the largest m2 is taken first, then the rescaled sums are added;
 // ex2.approx and lg2.approx move the result by about 1e-7 relative.
-__device__ __forceinline__ void chunk_row_lse(const ScoreArgs& a, const ItemTC& it, int row, int rows_c, int nsplit1,
-                                              float& nlse, int& tq) {
-  float l2 = INFINITY;
-  int t = -1;
+// The part of a row's merge that reads only the parameters (and tables
+// written before pass 1): the address of its first partial and its query
+// position (t = -1: no row).  Pass 2 does it before waiting for pass 1.
+struct LseRow {
+  const float2* src;
+  int t;
+};
+
+__device__ __forceinline__ LseRow lse_row_prep(const ScoreArgs& a, const ItemTC& it, int row, int rows_c, int nsplit1) {
+  LseRow p{nullptr, -1};
   if (row < rows_c) {
-    t = it.L - a.n + (it.qc * a.QC + row) % a.n;
-    const float2* src = a.p1part + pass1_item_index(a, it.r, it.g, it.qc, nsplit1) * a.QC + row;
-    const int64_t split_stride = (int64_t)a.NQC * a.QC;   // consecutive splits of one (g, qc)
+    p.t = it.L - a.n + (it.qc * a.QC + row) % a.n;
+    p.src = a.p1part + pass1_item_index(a, it.r, it.g, it.qc, nsplit1) * a.QC + row;
+  }
+  return p;
+}
+
+// The merge itself (split_stride: consecutive splits of one (g, qc)).
+__device__ __forceinline__ void lse_row_finish(const LseRow& p, int nsplit1, int64_t split_stride, float& nlse,
+                                               int& tq) {
+  float l2 = INFINITY;
+  int t = p.t;
+  if (p.src) {
+    const float2* src = p.src;
     float mm = -INFINITY, Z = 0.f;
     for (int s0 = 0; s0 < nsplit1; s0 += 24) {
       float2 pp[24];
@@ -119,6 +135,11 @@ __device__ __forceinline__ void chunk_row_lse(const ScoreArgs& a, const ItemTC& 
   }
   nlse = -l2;
   tq = t;
+}
+
+__device__ __forceinline__ void chunk_row_lse(const ScoreArgs& a, const ItemTC& it, int row, int rows_c, int nsplit1,
+                                              float& nlse, int& tq) {
+  lse_row_finish(lse_row_prep(a, it, row, rows_c, nsplit1), nsplit1, (int64_t)a.NQC * a.QC, nlse, tq);
 }
 
 // With carried tables, one warp of pass 1's first CTA does what

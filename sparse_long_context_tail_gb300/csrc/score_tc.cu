@@ -725,13 +725,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       else issue_mma<false>(a, sm, geo, ntiles, U, tmem, true, false, false);
     }
   } else {
-    if (early) pdl_wait();
     // lse2 of every query row of the chunk from the pass-1 partials (all key
     // splits), stored negated; -inf marks rows that do not exist (padding,
     // or positions before the request start).  The MMA runs meanwhile: the
-    // first unit is not read before this is done.
+    // first unit is not read before this is done.  The parameter reads come
+    // before the wait (a chunk has at most kEpiThreads rows).
     const int nsplit1 = ceil_div_dev(it.L, a.KS1);
-    for (int row = tid; row < qcols; row += kEpiThreads)
+    const int64_t split_stride = (int64_t)a.NQC * a.QC;
+    const LseRow mine = tid < qcols ? lse_row_prep(a, it, tid, rows_c, nsplit1) : LseRow{nullptr, -1};
+    if (early) pdl_wait();
+    if (tid < qcols) lse_row_finish(mine, nsplit1, split_stride, sm.nlse[tid], sm.tq[tid]);
+    for (int row = tid + kEpiThreads; row < qcols; row += kEpiThreads)
       chunk_row_lse(a, it, row, rows_c, nsplit1, sm.nlse[row], sm.tq[row]);
     epi_bar();
     if (geo.unit_cols == 256) pass2_epilogue<2>(a, sm, geo, it, U, k0, k1, ntiles, tmem, warp, lane);

@@ -328,18 +328,34 @@ __global__ void __launch_bounds__(kGatherThreads) gather_list_kernel(const __gri
     s_nblk0 = 0;
   }
   pdl_trigger();
-  pdl_wait();
   const CompactArgs& a = g.c;
-  const DescView dv = gather_view(g);
   const int lane = threadIdx.x & 31;
+  // With the descriptor in the parameters, the prologue's addresses come from
+  // the parameters alone and are worked out before the wait for the tail.
+  const bool early = g.desc.R > 0;
+  const int32_t *p_off = nullptr, *p_blk = nullptr;
+  if (early && threadIdx.x < 32 && lane < g.desc.blk[1] - g.desc.blk[0]) {
+    p_off = g.kept_off + g.desc.blk[0] + lane;
+    p_blk = g.kept_blk + g.desc.blk[0] + lane;
+  }
+  const int32_t* p_total = a.total_kept;
+  const int32_t* p_nblk0 = g.kept_nblk;
+  pdl_wait();
+  const DescView dv = gather_view(g);
   if (threadIdx.x < 32 && a.R > 0) {
-    const int base0 = dv.blk[0], nb0 = dv.blk[1] - base0;
-    int off = INT_MAX, blk = 0;
-    if (lane < nb0) {   // inside request 0's block range; entries past its count are unused
-      off = g.kept_off[base0 + lane];
-      blk = g.kept_blk[base0 + lane];
+    if (!early) {
+      const int base0 = dv.blk[0], nb0 = dv.blk[1] - base0;
+      if (lane < nb0) {   // inside request 0's block range; entries past its count are unused
+        p_off = g.kept_off + base0 + lane;
+        p_blk = g.kept_blk + base0 + lane;
+      }
     }
-    const int total = *a.total_kept, nblk0 = g.kept_nblk[0];
+    int off = INT_MAX, blk = 0;
+    if (p_off) {
+      off = *p_off;
+      blk = *p_blk;
+    }
+    const int total = *p_total, nblk0 = *p_nblk0;
     s_off0[lane] = off;
     s_blk0[lane] = blk;
     if (lane == 0) {
