@@ -10,16 +10,22 @@
 // so totals and histograms are exact integer sums (deterministic in any
 // order; rounding below 1e-10 of the total).  Non-negative float bit patterns
 // order like the values, so an MSB-first radix select over the 32-bit
-// patterns (8 bits per round, integer mass histograms in shared memory) finds
-// the score v* of the last block needed; blocks above v* are in, blocks equal
-// to v* enter in index order until the mass is reached.  No sort.
+// patterns (8 bits per round, integer mass and count histograms in shared
+// memory) narrows down the bucket holding the boundary: the block whose mass
+// brings the ranked prefix (score desc, index asc) to p of the total.  Blocks
+// above the bucket are in.  Once the bucket holds at most kCountSel blocks
+// (usually after the first round) its blocks are listed and each is kept when
+// the mass ranked before it is below the target, counted by one thread per
+// candidate; a bucket that never gets that small (many equal scores) ends
+// after four rounds with one score v*, whose blocks enter in index order
+// until the mass is reached.  No sort.
 //
-// Histogram updates are aggregated per warp before the shared-memory atomic:
+// Histogram updates are aggregated per warp before the shared-memory atomics:
 // the blocks of a request have similar magnitudes, so in the first rounds most
 // of them share a few digits, and one atomic per block would serialise on
-// those few addresses.  Lanes with equal digits (match.any) sum their masses
-// with two 32-bit warp reductions (24-bit halves, so no sum overflows) and one
-// lane adds the group's total.
+// those few addresses.  Lanes with the digit of the lowest pending lane add
+// their masses with full-warp reductions of the masses' 16-bit parts, and one
+// lane adds the group's sums and count.
 #pragma once
 
 #include <cmath>
@@ -30,7 +36,7 @@ namespace upf {
 
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kCountSel = 256;   // requests of up to this many blocks are ranked by counting
+constexpr int kCountSel = 256;   // requests (and boundary buckets) of up to this many blocks are ranked by counting
 
 // Shared memory the select core needs beyond its static arrays, for a request
 // of up to nbp blocks (nbp a multiple of 8).
