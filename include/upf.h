@@ -174,12 +174,14 @@ size_t upf_workspace_bytes(const upf_batch* batch, const upf_params* params);
 
 /* Work split of the two scoring passes for this batch (inspection and tests;
  * no GPU needed): keys per split of pass 1 and pass 2, the number of work
- * items of each pass, and the CTAs that run one item (1, or 2 for a CTA pair
- * sharing M = 256 MMAs).  Any output may be NULL.  The tensor-core passes run
- * one CTA per SM, so the split is chosen by the estimated time of the items
- * over the device's 152 SMs (76 pairs).  Errors: as upf_workspace_bytes. */
+ * items of each pass, and the CTAs that run one item of each pass (1, or 2
+ * for a CTA pair sharing M = 256 MMAs; the passes may differ, and then pass 2
+ * runs one query chunk per two of pass 1).  Any output may be NULL.  The
+ * tensor-core passes run one CTA per SM, so the split is chosen by the
+ * estimated time of the items over the device's 152 SMs (76 pairs).  Errors:
+ * as upf_workspace_bytes. */
 upf_status upf_plan_info(const upf_batch* batch, const upf_params* params, int32_t* key_split1, int32_t* key_split2,
-                         int64_t* items1, int64_t* items2, int32_t* ctas_per_item);
+                         int64_t* items1, int64_t* items2, int32_t* ctas_per_item1, int32_t* ctas_per_item2);
 
 /* Tail-query importance of every token (section 二, first step; section 三,
  * scores + online normalisation):

@@ -62,7 +62,7 @@ _SIGNATURES = {
                          c_int64, c_void_p, c_void_p, c_size_t, c_void_p], c_int),
     "upf_set_wait_limit": ([c_void_p, c_int64], c_int),
     "upf_plan_info": ([POINTER(UpfBatch), POINTER(UpfParams), POINTER(c_int32), POINTER(c_int32), POINTER(c_int64),
-                       POINTER(c_int64), POINTER(c_int32)], c_int),
+                       POINTER(c_int64), POINTER(c_int32), POINTER(c_int32)], c_int),
     "upf_select": ([c_void_p, POINTER(UpfBatch), POINTER(UpfParams), c_void_p, c_void_p, c_void_p, c_void_p,
                     c_void_p, c_size_t, c_void_p], c_int),
     "upf_compact": ([c_void_p, POINTER(UpfBatch), c_void_p, POINTER(UpfCompactIO), c_void_p, c_size_t, c_void_p],
@@ -187,11 +187,12 @@ def upf_score_shard(ctx, batch, params, num_q_heads_total, q, q_row_stride, k, k
 
 
 def upf_plan_info(batch: UpfBatch, params: UpfParams):
-    """(keys per split of pass 1, of pass 2, items of pass 1, items of pass 2, CTAs per item)."""
-    k1, k2, i1, i2, c = c_int32(), c_int32(), c_int64(), c_int64(), c_int32()
+    """(keys per split of pass 1, of pass 2, items of pass 1, items of pass 2,
+    CTAs per item of pass 1, of pass 2)."""
+    k1, k2, i1, i2, c1, c2 = c_int32(), c_int32(), c_int64(), c_int64(), c_int32(), c_int32()
     _check(load().upf_plan_info(ctypes.byref(batch), ctypes.byref(params), ctypes.byref(k1), ctypes.byref(k2),
-                                ctypes.byref(i1), ctypes.byref(i2), ctypes.byref(c)))
-    return k1.value, k2.value, i1.value, i2.value, c.value
+                                ctypes.byref(i1), ctypes.byref(i2), ctypes.byref(c1), ctypes.byref(c2)))
+    return k1.value, k2.value, i1.value, i2.value, c1.value, c2.value
 
 
 def upf_set_wait_limit(ctx: int, cycles: int) -> None:

@@ -77,8 +77,8 @@ __device__ __forceinline__ ItemTC locate_item(const ScoreArgs& a, int item, bool
   return locate_tc(pass2 ? a.item_off2 : a.item_off1, a.cu, a.R, item, pass2 ? a.KS2 : a.KS1, a.NQC);
 }
 __device__ __forceinline__ int64_t pass1_item_index(const ScoreArgs& a, int r, int g, int qc, int nsplit1) {
-  if (a.desc.R > 0) return item_index(a.desc.off1, r, g, 0, qc, nsplit1, a.NQC);
-  return item_index(a.item_off1, r, g, 0, qc, nsplit1, a.NQC);
+  if (a.desc.R > 0) return item_index(a.desc.off1, r, g, 0, qc, nsplit1, a.NQC1);
+  return item_index(a.item_off1, r, g, 0, qc, nsplit1, a.NQC1);
 }
 
 // Pass 2's entry for chunk row `row` of item it: -lse2 of the row's query,
@@ -99,8 +99,10 @@ struct LseRow {
 __device__ __forceinline__ LseRow lse_row_prep(const ScoreArgs& a, const ItemTC& it, int row, int rows_c, int nsplit1) {
   LseRow p{nullptr, -1};
   if (row < rows_c) {
-    p.t = it.L - a.n + (it.qc * a.QC + row) % a.n;
-    p.src = a.p1part + pass1_item_index(a, it.r, it.g, it.qc, nsplit1) * a.QC + row;
+    const int gr = it.qc * a.QC + row;   // row of the group; pass 1 may cut the group into smaller chunks
+    const int qc1 = a.QC1 == a.QC ? it.qc : gr / a.QC1;
+    p.t = it.L - a.n + gr % a.n;
+    p.src = a.p1part + pass1_item_index(a, it.r, it.g, qc1, nsplit1) * a.QC1 + (gr - qc1 * a.QC1);
   }
   return p;
 }
@@ -139,7 +141,7 @@ __device__ __forceinline__ void lse_row_finish(const LseRow& p, int nsplit1, int
 
 __device__ __forceinline__ void chunk_row_lse(const ScoreArgs& a, const ItemTC& it, int row, int rows_c, int nsplit1,
                                               float& nlse, int& tq) {
-  lse_row_finish(lse_row_prep(a, it, row, rows_c, nsplit1), nsplit1, (int64_t)a.NQC * a.QC, nlse, tq);
+  lse_row_finish(lse_row_prep(a, it, row, rows_c, nsplit1), nsplit1, (int64_t)a.NQC1 * a.QC1, nlse, tq);
 }
 
 // With carried tables, one warp of pass 1's first CTA does what

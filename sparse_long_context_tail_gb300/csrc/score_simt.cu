@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(32) describe_kernel(const DescribeArgs a) {
       bad |= L < 0;
       const int Lc = L < 0 ? 0 : L;
       v[0] = a.Hkv * a.NQC * ceil_div_dev(Lc, a.KS1);
-      v[1] = a.Hkv * a.NQC * ceil_div_dev(Lc, a.KS2);
+      v[1] = a.Hkv * a.NQC2 * ceil_div_dev(Lc, a.KS2);
       v[2] = ceil_div_dev(Lc, a.G);
     }
     int incl[3] = {v[0], v[1], v[2]};

@@ -731,7 +731,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     // first unit is not read before this is done.  The parameter reads come
     // before the wait (a chunk has at most kEpiThreads rows).
     const int nsplit1 = ceil_div_dev(it.L, a.KS1);
-    const int64_t split_stride = (int64_t)a.NQC * a.QC;
+    const int64_t split_stride = (int64_t)a.NQC1 * a.QC1;   // consecutive pass-1 splits of one (g, qc)
     const LseRow mine = tid < qcols ? lse_row_prep(a, it, tid, rows_c, nsplit1) : LseRow{nullptr, -1};
     if (early) pdl_wait();
     if (tid < qcols) lse_row_finish(mine, nsplit1, split_stride, sm.nlse[tid], sm.tq[tid]);

@@ -118,7 +118,7 @@ extern "C" upf_status upf_select_noalloc(const upf_batch* batch, const upf_param
   da.R = R;
   da.T = cu[R];
   da.Hkv = 1;
-  da.NQC = 1;
+  da.NQC = da.NQC2 = 1;
   da.KS1 = da.KS2 = 1 << 30;
   da.G = params->block;
   da.items1 = da.items2 = nonempty;

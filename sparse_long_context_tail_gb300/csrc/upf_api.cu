@@ -82,10 +82,12 @@ struct Plan {
   int n = 0, G = 0, sink = 0, tail = 0;
   float top_p = 0.f, scale = 0.f;
   int QR = 0, QC = 0, NQC = 0, KS1 = 0, KS2 = 0;
+  int QC2 = 0, NQC2 = 0;   // pass 2's query chunks (QC2 a multiple of QC)
   int pw = 1;   // partial rows per pass-1 item row and per (kv head, query chunk)
   int q_box_rows = 0;
   bool use_tc = false;
-  bool use_pair = false;
+  bool use_pair = false;    // pass 1 on CTA pairs
+  bool use_pair2 = false;   // pass 2 on CTA pairs
   long long items1 = 0, items2 = 0;
   long long NB = 0;
   int max_nb = 0;
@@ -353,12 +355,27 @@ upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p
     // slower, so those stay on single CTAs.  UPF_SCORE_PAIRS=0 keeps every
     // chunk on single CTAs, =1 allows pairs at any d (tests cross-check both).
     pl->use_pair = pl->use_tc && pl->QC % 256 == 0 && !pairs_off && (pl->d == 256 || pairs_any_d);
-    if (pl->use_pair) {
-      pl->KS1 = choose_split_tc(b, pl->Hkv, pl->NQC, upf::kPairTileKeys, upf::kPlanSMs / 2);
-      pl->KS2 = choose_split_tc(b, pl->Hkv, pl->NQC, upf::kPairTileKeys, upf::kPlanSMs / 2);
-    } else if (pl->use_tc) {
-      pl->KS1 = choose_split_tc(b, pl->Hkv, pl->NQC, upf::score_tc_key_tile(1, pl->d), upf::kPlanSMs);
-      pl->KS2 = choose_split_tc(b, pl->Hkv, pl->NQC, upf::score_tc_key_tile(2, pl->d), upf::kPlanSMs);
+    pl->QC2 = pl->QC;
+    pl->NQC2 = pl->NQC;
+    pl->use_pair2 = pl->use_pair;
+    // A d = 256 group of 129..256 rows in a long pass: pass 1 on single CTAs
+    // in 128-row chunks (above), pass 2 on CTA pairs in one 256-row chunk that
+    // merges both pass-1 chunks' partials.  Measured per pass against one
+    // layout for both (Gemma-3 n = 128, 8 kv heads x 128K keys): pass 1 126.5
+    // us single against 139 on pairs, pass 2 134 on pairs against 141.4
+    // single, step 280 -> 273 us.  With 2 kv heads (Qwen3-Next n = 32) pass 2
+    // gained 0.8 us and the step lost 1.6, so shorter passes keep one layout.
+    if (pl->use_tc && pl->d == 256 && !pairs_off && pl->QC == 128 && pl->QR > 128 && pl->QR <= 256 &&
+        (long long)pl->Hkv * pl->T >= (1LL << 19)) {
+      pl->QC2 = 256;
+      pl->NQC2 = 1;
+      pl->use_pair2 = true;
+    }
+    if (pl->use_tc) {
+      pl->KS1 = pl->use_pair ? choose_split_tc(b, pl->Hkv, pl->NQC, upf::kPairTileKeys, upf::kPlanSMs / 2)
+                             : choose_split_tc(b, pl->Hkv, pl->NQC, upf::score_tc_key_tile(1, pl->d), upf::kPlanSMs);
+      pl->KS2 = pl->use_pair2 ? choose_split_tc(b, pl->Hkv, pl->NQC2, upf::kPairTileKeys, upf::kPlanSMs / 2)
+                              : choose_split_tc(b, pl->Hkv, pl->NQC2, upf::score_tc_key_tile(2, pl->d), upf::kPlanSMs);
     } else {
       pl->KS1 = choose_split(b, pl->Hkv * pl->NQC, 4LL * upf::kPlanSMs, 128);
       pl->KS2 = choose_split(b, pl->Hkv * pl->NQC, 4LL * upf::kPlanSMs, 128);
@@ -370,7 +387,7 @@ upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p
     for (int r = 0; r < pl->R; ++r) {
       int L = b->cu_seqlens_host[r + 1] - b->cu_seqlens_host[r];
       pl->items1 += (long long)pl->Hkv * pl->NQC * ceil_div(L, pl->KS1);
-      pl->items2 += (long long)pl->Hkv * pl->NQC * ceil_div(L, pl->KS2);
+      pl->items2 += (long long)pl->Hkv * pl->NQC2 * ceil_div(L, pl->KS2);
       int nb = ceil_div(L, pl->G);
       pl->NB += nb;
       pl->max_nb = std::max(pl->max_nb, nb);
@@ -394,7 +411,7 @@ upf_status make_plan(const upf_ctx* ctx, const upf_batch* b, const upf_params* p
   pl->off_p1 = off;
   off = align256(off + sizeof(float2) * size_t(pl->items1) * pl->pw * pl->QC);
   pl->off_part = off;
-  off = align256(off + sizeof(float) * size_t(pl->Hkv) * pl->NQC * pl->pw * pl->T);
+  off = align256(off + sizeof(float) * size_t(pl->Hkv) * pl->NQC2 * pl->pw * pl->T);
   pl->off_bs = off;
   off = align256(off + sizeof(float) * size_t(pl->NB));
   pl->off_chunk = off;
@@ -502,8 +519,10 @@ upf::ScoreArgs score_args(const upf_ctx* ctx, const upf_batch* b, const Plan& pl
   a.n = pl.n;
   a.gamma = pl.gamma;
   a.QR = pl.QR;
-  a.QC = pl.QC;
+  a.QC = pl.QC;     // pass 1's chunks; pass2_args() switches to pass 2's
   a.NQC = pl.NQC;
+  a.QC1 = pl.QC;
+  a.NQC1 = pl.NQC;
   a.KS1 = pl.KS1;
   a.KS2 = pl.KS2;
   a.items1 = int(pl.items1);
@@ -523,6 +542,16 @@ upf::ScoreArgs score_args(const upf_ctx* ctx, const upf_batch* b, const Plan& pl
   return a;
 }
 
+// Pass 2's arguments: pass 1's with pass 2's query chunks and kernel kind
+// (QC1 / NQC1 keep pass 1's, where the pass-1 partials are).
+upf::ScoreArgs pass2_args(const upf::ScoreArgs& a1, const Plan& pl) {
+  upf::ScoreArgs a = a1;
+  a.QC = pl.QC2;
+  a.NQC = pl.NQC2;
+  a.use_pair = pl.use_pair2 ? 1 : 0;
+  return a;
+}
+
 upf::DescribeArgs describe_args(const upf_ctx* ctx, const upf_batch* b, const Plan& pl, void* ws) {
   upf::DescribeArgs a;
   a.cu = b->cu_seqlens_dev;
@@ -530,6 +559,7 @@ upf::DescribeArgs describe_args(const upf_ctx* ctx, const upf_batch* b, const Pl
   a.T = pl.T;
   a.Hkv = pl.Hkv;
   a.NQC = pl.NQC;
+  a.NQC2 = pl.NQC2;
   a.KS1 = pl.KS1;
   a.KS2 = pl.KS2;
   a.G = pl.G;
@@ -549,7 +579,7 @@ upf::DescribeArgs describe_args(const upf_ctx* ctx, const upf_batch* b, const Pl
 // at most kInlineReqs requests).
 void fill_desc(const upf_batch* b, const Plan& pl, upf::DescInline* d) {
   const int32_t* cu = b->cu_seqlens_host;
-  const int units = pl.Hkv * pl.NQC;
+  const int units1 = pl.Hkv * pl.NQC, units2 = pl.Hkv * pl.NQC2;
   int o1 = 0, o2 = 0, ob = 0;
   d->R = pl.R;
   for (int r = 0; r <= pl.R; ++r) {
@@ -559,8 +589,8 @@ void fill_desc(const upf_batch* b, const Plan& pl, upf::DescInline* d) {
     d->blk[r] = ob;
     if (r == pl.R) break;
     const int L = cu[r + 1] - cu[r];
-    o1 += units * ceil_div(L, pl.KS1);
-    o2 += units * ceil_div(L, pl.KS2);
+    o1 += units1 * ceil_div(L, pl.KS1);
+    o2 += units2 * ceil_div(L, pl.KS2);
     ob += ceil_div(L, pl.G);
   }
 }
@@ -839,8 +869,8 @@ static upf_status score_impl(upf_ctx* ctx, const upf_batch* batch, const upf_par
   UPF_LAUNCH(staged(ctx, kDescribe, s, [&] { return upf::launch_describe(da, s, false); }), "describe");
   upf::ScoreArgs sa = score_args(ctx, batch, pl, q, q_row_stride, k, k_row_stride, ws);
   UPF_LAUNCH(staged(ctx, kPass1, s, [&] { return upf::launch_score_pass1(sa, s, true); }), "score pass 1");
-  UPF_LAUNCH(staged(ctx, kPass2, s, [&] { return upf::launch_score_pass2(sa, s, true); }), "score pass 2");
-  upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC * pl.pw, sa.part, nullptr, scores, nullptr,
+  UPF_LAUNCH(staged(ctx, kPass2, s, [&] { return upf::launch_score_pass2(pass2_args(sa, pl), s, true); }), "score pass 2");
+  upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC2 * pl.pw, sa.part, nullptr, scores, nullptr,
                                    nullptr, nullptr);
   se.Hq = hq_norm;
   UPF_LAUNCH(staged(ctx, kFinalize, s, [&] { return upf::launch_block_means(se, s, true); }), "finalize scores");
@@ -848,7 +878,7 @@ static upf_status score_impl(upf_ctx* ctx, const upf_batch* batch, const upf_par
 }
 
 upf_status upf_plan_info(const upf_batch* batch, const upf_params* params, int32_t* key_split1, int32_t* key_split2,
-                         int64_t* items1, int64_t* items2, int32_t* ctas_per_item) {
+                         int64_t* items1, int64_t* items2, int32_t* ctas_per_item1, int32_t* ctas_per_item2) {
   Plan pl;
   upf_status st = make_plan(nullptr, batch, params, true, &pl);
   if (st != UPF_OK) return st;
@@ -856,7 +886,8 @@ upf_status upf_plan_info(const upf_batch* batch, const upf_params* params, int32
   if (key_split2) *key_split2 = pl.KS2;
   if (items1) *items1 = pl.items1;
   if (items2) *items2 = pl.items2;
-  if (ctas_per_item) *ctas_per_item = pl.use_pair ? 2 : 1;
+  if (ctas_per_item1) *ctas_per_item1 = pl.use_pair ? 2 : 1;
+  if (ctas_per_item2) *ctas_per_item2 = pl.use_pair2 ? 2 : 1;
   return UPF_OK;
 }
 
@@ -990,8 +1021,8 @@ upf_status upf_select_tokens(upf_ctx* ctx, const upf_batch* batch, const upf_par
     UPF_LAUNCH(staged(ctx, kDescribe, s, [&] { return upf::launch_describe(da, s, false); }), "describe");
   }
   UPF_LAUNCH(staged(ctx, kPass1, s, [&] { return upf::launch_score_pass1(sa, s, true); }), "score pass 1");
-  UPF_LAUNCH(staged(ctx, kPass2, s, [&] { return upf::launch_score_pass2(sa, s, true); }), "score pass 2");
-  upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC * pl.pw, sa.part, nullptr, scores, block_scores,
+  UPF_LAUNCH(staged(ctx, kPass2, s, [&] { return upf::launch_score_pass2(pass2_args(sa, pl), s, true); }), "score pass 2");
+  upf::SelectArgs se = select_args(ctx, batch, pl, ws, pl.Hkv * pl.NQC2 * pl.pw, sa.part, nullptr, scores, block_scores,
                                    keep_bits, kept_count);
   if (fused_tail(pl)) {
     // finalize + block means + select + kept-block lists + compacted offsets

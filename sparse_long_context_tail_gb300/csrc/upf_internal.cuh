@@ -65,7 +65,8 @@ struct ScoreArgs {
   int64_t k_stride;      // elements between consecutive tokens of k
   const int32_t* cu;     // device cu_seqlens [R+1]
   int32_t R, T, Hq, Hkv, d, n, gamma;
-  int32_t QR, QC, NQC;
+  int32_t QR, QC, NQC;      // this pass's query chunks: NQC chunks of QC rows per group
+  int32_t QC1, NQC1;        // pass 1's chunks (where pass 2 reads the pass-1 partials); QC is a multiple of QC1
   int32_t KS1, KS2;
   int32_t items1, items2;  // host totals (grid sizes)
   float scale_log2;
@@ -75,7 +76,7 @@ struct ScoreArgs {
   const int32_t* item_off1;  // [R+1]
   const int32_t* item_off2;  // [R+1]
   float2* p1part;            // [items1][pw][QC]
-  float* part;               // [Hkv*NQC*pw][T]
+  float* part;               // [Hkv*NQC*pw][T] (pass 2's NQC)
   int32_t pw;                // partial rows per item row / per (g, qc): kTcPartials or 1
   int32_t* status;
   long long wait_limit;      // pipeline waits of the tensor-core kernels (cycles)
@@ -87,7 +88,7 @@ struct ScoreArgs {
 
 struct DescribeArgs {
   const int32_t* cu;
-  int32_t R, T, Hkv, NQC, KS1, KS2, G;
+  int32_t R, T, Hkv, NQC, NQC2, KS1, KS2, G;   // NQC, NQC2: query chunks per group of pass 1, pass 2
   int32_t items1, items2, NB;  // host totals: the device-derived ones must match
   int32_t* item_off1;
   int32_t* item_off2;

@@ -130,9 +130,7 @@ def test_scoring_work_split_is_near_the_best_whole_tile_split(lib):
         cu = np.concatenate([[0], np.cumsum(s.lengths)]).astype(np.int32)
         b, keep = B.make_batch(0x1000, cu, s.num_q_heads, s.num_kv_heads, s.head_dim)
         p = B.make_params(s.n_tail, s.block, s.sink_keep, s.tail_keep, s.top_p)
-        ks1, ks2, n1, n2, ctas = B.upf_plan_info(b, p)
-        assert ctas in (1, 2)
-        sms = 152 // ctas
+        ks1, ks2, n1, n2, ctas1, ctas2 = B.upf_plan_info(b, p)
         gamma = s.num_q_heads // s.num_kv_heads
         qr = gamma * s.n_tail
         qc = min(-(-qr // 128) * 128, 512 if s.head_dim <= 128 else (128 if qr <= 256 else 256))
@@ -141,13 +139,23 @@ def test_scoring_work_split_is_near_the_best_whole_tile_split(lib):
         while qc > 128 and s.num_kv_heads * -(-qr // qc) * sum(-(-L // tile1) for L in s.lengths) < 152:
             qc = -(-(qc // 2) // 128) * 128
         nqc = -(-qr // qc)
-        units = s.num_kv_heads * nqc
-        for ks, n, tile in ((ks1, n1, 256 if ctas == 2 or s.head_dim <= 128 else 128),
-                            (ks2, n2, 256 if ctas == 2 else 128)):
+        # pairs when the chunk is whole 256-row units at d = 256; a d = 256
+        # group of 129..256 rows in a long pass (kv heads x tokens >= 2^19)
+        # runs pass 1 in two 128-row chunks on single CTAs and pass 2 in one
+        # 256-row chunk on pairs
+        pair1 = s.head_dim == 256 and qc % 256 == 0
+        split = (s.head_dim == 256 and qc == 128 and 128 < qr <= 256
+                 and s.num_kv_heads * sum(s.lengths) >= 1 << 19)
+        assert (ctas1, ctas2) == ((2 if pair1 else 1), (2 if pair1 or split else 1)), name
+        nqc2 = 1 if split else nqc
+        for ks, n, tile, nq, ctas in ((ks1, n1, 256 if ctas1 == 2 or s.head_dim <= 128 else 128, nqc, ctas1),
+                                      (ks2, n2, 256 if ctas2 == 2 else 128, nqc2, ctas2)):
+            sms = 152 // ctas
+            units = s.num_kv_heads * nq
             assert ks % tile == 0 and ks >= 256, (name, ks)
             assert n == units * sum(-(-L // ks) for L in s.lengths), name
             ovh = 2 * tile
             lo = max(256, -(-sum(s.lengths) * units // (4 * sms) // tile) * tile)
             cand = range(lo, -(-max(s.lengths) // tile) * tile + tile, tile)
-            best = min(_greedy_makespan(s.lengths, s.num_kv_heads, nqc, c, ovh, sms) for c in cand)
-            assert _greedy_makespan(s.lengths, s.num_kv_heads, nqc, ks, ovh, sms) <= 1.02 * best, (name, ks)
+            best = min(_greedy_makespan(s.lengths, s.num_kv_heads, nq, c, ovh, sms) for c in cand)
+            assert _greedy_makespan(s.lengths, s.num_kv_heads, nq, ks, ovh, sms) <= 1.02 * best, (name, ks)

@@ -115,6 +115,9 @@ SMALL = [
     ("llama-2req", dict(lengths=[3000, 1700], H=(32, 8, 128), hidden=4096, n=128, G=64, planted=[4, 2])),
     ("qwen-n512-G32", dict(lengths=[2500], H=(16, 2, 256), hidden=2048, n=512, G=32, planted=[5])),
     ("gemma-n32-G128", dict(lengths=[2000, 640], H=(16, 8, 256), hidden=3840, n=32, G=128, planted=[2, 1])),
+    # 256 rows per group at d = 256 over 8 kv heads x 65536+ tokens: pass 1 in two 128-row chunks,
+    # pass 2 in one 256-row chunk on CTA pairs
+    ("d256-rows256", dict(lengths=[40000, 0, 25600], H=(16, 8, 256), hidden=512, n=128, G=64, planted=[2, 0, 1])),
     ("tail-only", dict(lengths=[100, 129, 257], H=(8, 2, 128), hidden=256, n=128, G=64, planted=[0, 0, 0])),
     ("odd-hidden", dict(lengths=[3333], H=(8, 1, 128), hidden=520, n=64, G=16, planted=[7])),
     # 384 query rows per chunk: pass-2 units of 128 columns, three per key tile
@@ -151,12 +154,14 @@ def test_cuda_core_fallback_parity(sel, name, c, monkeypatch):
 
 
 @pytest.mark.parametrize("pairs", ["0", "1"])
-@pytest.mark.parametrize("name,c", [SMALL[1], SMALL[2], SMALL[0]], ids=["llama-2req", "qwen-n512-G32", "ragged-d64"])
+@pytest.mark.parametrize("name,c", [SMALL[1], SMALL[2], SMALL[0], SMALL[4]],
+                         ids=["llama-2req", "qwen-n512-G32", "ragged-d64", "d256-rows256"])
 def test_scoring_on_single_ctas_and_on_pairs(sel, name, c, pairs, monkeypatch):
-    """d = 256 chunks of whole 256-row units run on CTA pairs by default, the
-    rest on single CTAs; both kernel families must match the oracle at every
-    head dim (UPF_SCORE_PAIRS=0: single CTAs only, =1: pairs wherever the
-    chunk allows)."""
+    """d = 256 chunks of whole 256-row units run on CTA pairs by default (and
+    a d = 256 group of 256 rows runs pass 2 on pairs after pass 1 on single
+    CTAs), the rest on single CTAs; both kernel families must match the oracle
+    at every head dim (UPF_SCORE_PAIRS=0: single CTAs only, =1: pairs wherever
+    the chunk allows)."""
     monkeypatch.setenv("UPF_SCORE_PAIRS", pairs)
     spec = small_spec(name, c)
     w = wl.generate(spec)
